@@ -1,0 +1,161 @@
+"""ctypes front end of the fp32 contract emulator (``contract_emulator.c``).
+
+TEST INFRASTRUCTURE ONLY.  Given fp32 logits, it reproduces the contract's
+tile partials, shard records, log-sum-exp and logprob bit for bit.  The
+tests feed it logits that are known exactly on the CPU (``exact_case``
+inputs), never values read back from the GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        f, i64, i32 = ctypes.c_float, ctypes.c_int64, ctypes.c_int
+        P = ctypes.c_void_p
+        L.emu_exp.restype = f
+        L.emu_exp.argtypes = [f]
+        L.emu_log.restype = f
+        L.emu_log.argtypes = [f]
+        L.emu_merge.restype = None
+        L.emu_merge.argtypes = [f, f, f, f, P, P]
+        L.emu_tile_ms.restype = None
+        L.emu_tile_ms.argtypes = [P, i32, P, P]
+        L.emu_tree.restype = None
+        L.emu_tree.argtypes = [P, P, i64, P, P]
+        L.emu_tree_nodes.restype = i32
+        L.emu_tree_nodes.argtypes = [i64, i32, P, P]
+        L.emu_tile_partials.restype = None
+        L.emu_tile_partials.argtypes = [P, i64, i64, P, P]
+        L.emu_linear_logprob.restype = i32
+        L.emu_linear_logprob.argtypes = [P, i64, i64, P, P, i32, P, P, P, P, P, P, P, P]
+        for name in ("emu_exp_sweep", "emu_log_sweep"):
+            fn = getattr(L, name)
+            fn.restype = None
+            fn.argtypes = [f, f, P, P, P]
+        L.emu_constants.restype = None
+        L.emu_constants.argtypes = [P]
+        _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def exp(x: float) -> np.float32:
+    return np.float32(lib().emu_exp(ctypes.c_float(x)))
+
+
+def log(x: float) -> np.float32:
+    return np.float32(lib().emu_log(ctypes.c_float(x)))
+
+
+def merge(m1, s1, m2, s2):
+    mo, so = ctypes.c_float(), ctypes.c_float()
+    lib().emu_merge(m1, s1, m2, s2, ctypes.byref(mo), ctypes.byref(so))
+    return np.float32(mo.value), np.float32(so.value)
+
+
+def tile_ms(v: np.ndarray):
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    assert 1 <= v.shape[0] <= 128
+    mo, so = ctypes.c_float(), ctypes.c_float()
+    lib().emu_tile_ms(_ptr(v), int(v.shape[0]), ctypes.byref(mo), ctypes.byref(so))
+    return np.float32(mo.value), np.float32(so.value)
+
+
+def tree(m: np.ndarray, s: np.ndarray):
+    m = np.ascontiguousarray(m, dtype=np.float32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    mo, so = ctypes.c_float(), ctypes.c_float()
+    lib().emu_tree(_ptr(m), _ptr(s), int(m.shape[0]), ctypes.byref(mo), ctypes.byref(so))
+    return np.float32(mo.value), np.float32(so.value)
+
+
+def tree_nodes(n_tiles: int, depth: int):
+    b = np.zeros(64, dtype=np.int64)
+    e = np.zeros(64, dtype=np.int64)
+    rc = lib().emu_tree_nodes(n_tiles, depth, _ptr(b), _ptr(e))
+    if rc != 0:
+        raise ValueError("tree too shallow")
+    k = 1 << depth
+    return list(zip(b[:k].tolist(), e[:k].tolist()))
+
+
+def tile_partials(logits: np.ndarray):
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, V = L.shape
+    nt = (V + 127) // 128
+    tm = np.empty((T, nt), dtype=np.float32)
+    ts = np.empty((T, nt), dtype=np.float32)
+    lib().emu_tile_partials(_ptr(L), T, V, _ptr(tm), _ptr(ts))
+    return tm, ts
+
+
+def linear_logprob(logits: np.ndarray, targets: np.ndarray, active: Optional[np.ndarray] = None,
+                   n_shards: int = 1):
+    """Contract outputs from fp32 logits [T, V].
+
+    Returns a dict: logprob, lse [T]; rec_m, rec_s, rec_tgt [n_shards, T];
+    rec_owned (uint32) [n_shards, T]; root_m, root_s [T] (tree taken
+    directly over all tiles, without the shard level).
+    """
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, V = L.shape
+    tg = np.ascontiguousarray(targets, dtype=np.int32)
+    act = None if active is None else np.ascontiguousarray(active, dtype=np.uint8)
+    out = {
+        "logprob": np.empty(T, np.float32), "lse": np.empty(T, np.float32),
+        "rec_m": np.empty((n_shards, T), np.float32), "rec_s": np.empty((n_shards, T), np.float32),
+        "rec_tgt": np.empty((n_shards, T), np.float32),
+        "rec_owned": np.empty((n_shards, T), np.uint32),
+        "root_m": np.empty(T, np.float32), "root_s": np.empty(T, np.float32),
+    }
+    rc = lib().emu_linear_logprob(_ptr(L), T, V, _ptr(tg), _ptr(act), n_shards,
+                                  _ptr(out["logprob"]), _ptr(out["lse"]),
+                                  _ptr(out["rec_m"]), _ptr(out["rec_s"]), _ptr(out["rec_tgt"]),
+                                  _ptr(out["rec_owned"]), _ptr(out["root_m"]), _ptr(out["root_s"]))
+    if rc != 0:
+        raise ValueError("unsupported shard count %d for V=%d" % (n_shards, V))
+    return out
+
+
+def exp_sweep(lo: float, hi: float):
+    mu, wx, cnt = ctypes.c_double(), ctypes.c_float(), ctypes.c_int64()
+    lib().emu_exp_sweep(lo, hi, ctypes.byref(mu), ctypes.byref(wx), ctypes.byref(cnt))
+    return mu.value, wx.value, cnt.value
+
+
+def log_sweep(lo: float, hi: float):
+    mu, wx, cnt = ctypes.c_double(), ctypes.c_float(), ctypes.c_int64()
+    lib().emu_log_sweep(lo, hi, ctypes.byref(mu), ctypes.byref(wx), ctypes.byref(cnt))
+    return mu.value, wx.value, cnt.value
+
+
+def constants():
+    out = np.zeros(16, dtype=np.float32)
+    lib().emu_constants(_ptr(out))
+    names = ["log2e", "ln2_hi", "ln2_lo", "shifter", "sqrt2"] + ["inv_fact%d" % k for k in range(8)] \
+        + ["two_thirds", "two_fifths", "two_elevenths"]
+    return dict(zip(names, out.tolist()))
+
+
+def exact_fp32_logits(logits_f64: np.ndarray) -> np.ndarray:
+    """Cast fp64 logits to fp32, asserting the cast is exact (exact_case inputs)."""
+    L32 = logits_f64.astype(np.float32)
+    if not np.array_equal(L32.astype(np.float64), logits_f64):
+        raise ValueError("logits are not exactly representable in fp32")
+    return L32
+

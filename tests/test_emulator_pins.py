@@ -1,0 +1,155 @@
+"""Pins of the fp32 contract emulator (oracle/contract_emulator.c).
+
+The emulator predicts the GPU's bits; these tests tie it to things outside
+itself: fp64 libm over every fp32 input of exp and log, exact rational
+values of the contract constants, exact sums where every term is exact, the
+hand-derived tile tree, and the fp64 oracle within the error the fp32
+arithmetic allows.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import emulator as E
+from oracle import linear_logprob as O
+from invariant_selected_token_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def test_constants_match_their_definitions():
+    g = json.load(open(os.path.join(GOLDEN, "contract_constants.json")))
+    c = E.constants()
+    for name in ("log2e", "ln2_hi", "ln2_lo", "shifter", "sqrt2"):
+        assert float.fromhex(g[name]) == c[name], name
+    for k in range(8):
+        assert float.fromhex(g["inv_fact%d" % k]) == c["inv_fact%d" % k], k
+    assert float.fromhex(g["two_over_3"]) == c["two_thirds"]
+    assert float.fromhex(g["two_over_5"]) == c["two_fifths"]
+    assert float.fromhex(g["two_over_11"]) == c["two_elevenths"]
+
+
+def test_exp_exhaustive_accuracy():
+    """Every fp32 x in [-86, 0]: |rlk_exp(x) - exp(x)| < 1 ulp (fp64 libm reference)."""
+    max_ulp, worst, count = E.exp_sweep(-86.0, 0.0)
+    assert count == (np.float32(-86.0).view(np.uint32) - np.uint32(0x80000000) + 1)
+    assert max_ulp < 1.0, (max_ulp, worst)
+
+
+def test_log_exhaustive_accuracy():
+    """Every fp32 s in [1, 2^21] (the range of a tile-tree sum): within 2 ulp of fp64 log."""
+    max_ulp, worst, count = E.log_sweep(1.0, 2.0 ** 21)
+    assert count == 21 * (1 << 23) + 1
+    assert max_ulp <= 2.0, (max_ulp, worst)
+
+
+def test_exp_log_special_values():
+    assert E.exp(0.0) == 1.0 and E.exp(-0.0) == 1.0
+    assert E.log(1.0) == 0.0
+    assert E.exp(-np.inf) == 0.0 and E.exp(-86.0001) == 0.0
+    assert E.exp(-86.0) > 0.0
+    assert E.log(2.0) == np.float32(math.log(2.0))
+    assert abs(E.log(151936.0) - math.log(151936.0)) <= 2 * np.spacing(np.float32(11.93))
+
+
+def test_merge_rule():
+    # equal maxima: exp(0) = 1 exactly, so s = RN(s1 + s2) and the order does not matter
+    m, s = E.merge(2.5, 3.0, 2.5, 1e-8)
+    assert m == 2.5 and s == np.float32(np.float32(3.0) + np.float32(1e-8))
+    assert E.merge(2.5, 1e-8, 2.5, 3.0) == (m, s)
+    # larger max wins; the smaller side is scaled by exp(lo - hi)
+    m, s = E.merge(-1.0, 2.0, 3.0, 5.0)
+    assert m == 3.0
+    assert abs(s - (5.0 + 2.0 * math.exp(-4.0))) <= 2 * np.spacing(np.float32(5.0))
+    assert E.merge(3.0, 5.0, -1.0, 2.0) == (m, s)
+
+
+def test_tile_absent_slots_and_counts():
+    # all columns equal: every e_c = exp(0) = 1, so s counts the real columns exactly
+    for n in range(1, 129):
+        m, s = E.tile_ms(np.full(n, 0.75, np.float32))
+        assert m == np.float32(0.75) and s == n
+
+
+def test_tile_pairwise_tree_order():
+    """Tree over column slots, not left-to-right: e = [1, u, u, u, ...] with u = 2^-24."""
+    u = np.float32(2.0 ** -24)
+    # logits giving e_0 = 1 and e_c = 2^-24 exactly: d = ln(2^-24) is not exact, so instead
+    # check the structure with s values through the tile tree of leaves (m equal):
+    m = np.zeros(4, np.float32)
+    s = np.array([1.0, u, u, u], np.float32)
+    # bisection of 4 leaves: (1 + u) + (u + u) = 1 + 2u (exact: 2u is representable, RN(1+u)=1)
+    _, tot = E.tree(m, s)
+    assert tot == np.float32(1.0) + np.float32(2 * u)
+    # a sequential sum would give ((1 + u) + u) + u = 1
+    assert np.float32(np.float32(np.float32(1.0 + u) + u) + u) == np.float32(1.0)
+
+
+def test_tree_nodes_match_hand_derivation():
+    g = json.load(open(os.path.join(GOLDEN, "tile_tree.json")))
+    for d, n in ((1, "2"), (2, "4"), (3, "8")):
+        sizes = [b - a for a, b in E.tree_nodes(1187, d)]
+        assert sizes == g["151936"][n]
+    # emulator and oracle derive the tree independently
+    for nt in (1, 2, 3, 8, 9, 37, 1187, 2048):
+        for d in range(0, 4):
+            if (1 << d) > nt:
+                continue
+            assert E.tree_nodes(nt, d) == O.tile_tree_nodes(nt, d), (nt, d)
+
+
+def test_shard_route_equals_direct_tree():
+    """Shard records merged in shard order give the root of the full tile tree, bit for bit."""
+    w = workloads.small_case(16, 64, 3000, seed=21)
+    L = O.logits(w.hidden, w.W).astype(np.float32)
+    for n in (1, 2, 4, 8):
+        out = E.linear_logprob(L, w.targets, n_shards=n)
+        r0 = E.linear_logprob(L, w.targets, n_shards=1)
+        assert np.array_equal(out["lse"].view(np.uint32), r0["lse"].view(np.uint32))
+        assert np.array_equal(out["logprob"].view(np.uint32), r0["logprob"].view(np.uint32))
+        assert np.array_equal(out["root_s"].view(np.uint32), r0["root_s"].view(np.uint32))
+        assert np.all(out["rec_owned"].sum(axis=0) == 1)
+
+
+@pytest.mark.parametrize("T,H,V,seed", [(64, 256, 1024, 0), (37, 128, 1000, 5), (9, 64, 129, 6),
+                                        (5, 64, 1, 7)])
+def test_emulator_vs_fp64_oracle(T, H, V, seed):
+    """fp32 contract result vs fp64 definition on the same fp32 logits.
+
+    Bound: each exp is within 1 ulp, each tree add and fma rounds once, so the
+    relative error of s is at most about (2 + log2(n_tiles) + 7) * 2^-24 ~ 1e-6;
+    log adds 2 ulp; lse then carries at most ~2e-6 absolute for |lse| < 20.
+    """
+    w = workloads.small_case(T, H, V, seed=seed)
+    L64 = O.logits(w.hidden, w.W)
+    L32 = L64.astype(np.float32)
+    lp_ref, lse_ref = O.lse_and_logprob_from_logits(L32.astype(np.float64), w.targets)
+    out = E.linear_logprob(L32, w.targets, n_shards=1)
+    assert np.all(np.abs(out["lse"] - lse_ref) <= 2e-6 * np.maximum(1.0, np.abs(lse_ref)))
+    assert np.all(np.abs(out["logprob"] - lp_ref) <= 4e-6 * np.maximum(1.0, np.abs(lse_ref)))
+
+
+def test_emulator_on_exact_inputs_matches_oracle():
+    w = workloads.exact_case(32, 256, 2000, seed=3, n_shards=4)
+    L64 = O.logits(w.hidden, w.W)
+    L32 = E.exact_fp32_logits(L64)
+    lp_ref, lse_ref = O.lse_and_logprob_from_logits(L64, w.targets)
+    out = E.linear_logprob(L32, w.targets, n_shards=4)
+    assert np.all(np.abs(out["lse"] - lse_ref) <= 2e-6 * np.maximum(1.0, np.abs(lse_ref)))
+    assert np.all(np.abs(out["logprob"] - lp_ref) <= 4e-6 * np.maximum(1.0, np.abs(lse_ref)))
+
+
+def test_inactive_and_unowned_rows():
+    w = workloads.small_case(4, 64, 300, seed=9)
+    L = O.logits(w.hidden, w.W).astype(np.float32)
+    tg = w.targets.copy()
+    tg[2] = 300
+    act = np.array([1, 0, 1, 1], np.uint8)
+    out = E.linear_logprob(L, tg, active=act, n_shards=2)
+    assert out["logprob"][1] == 0.0 and out["lse"][1] == 0.0
+    assert np.all(out["rec_owned"][:, 1] == 0) and np.all(out["rec_s"][:, 1] == 0)
+    assert np.isnan(out["logprob"][2]) and np.isnan(out["lse"][2])
+    assert np.isfinite(out["logprob"][3])
