@@ -1,0 +1,351 @@
+"""Throughput of the selected-token logprob on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rlk|reference]
+
+One step = one pass of the whole path over one packed batch of the
+Qwen3-8B-shaped head (T=4096 tokens = 8 x 512, H=4096, V=151936, bf16, 4
+vocabulary shards): the logits GEMM with the fused tile epilogue, then the
+tile tree, shard records and final lse/logprob.  Inputs are synthetic and
+seeded (see invariant_selected_token_gb300/workloads.py) and resident in HBM
+before the timed region; W (1.24 GB) is larger than L2, so no flush is
+needed between steps.  Prints one JSON line (rank 0).
+
+With --gpus N > 1 (launched by torchrun) each rank runs its own independent
+batch against its own copy of W -- the path shards over tokens with no data
+exchange -- and `value` is the tokens of all ranks over the slowest rank's
+time (weak scaling).
+
+--impl reference times the fp64 CPU oracle on the host cores instead
+(bounded samples of the same batch), on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+H, V, T_PACKED, N_SHARDS = 4096, 151936, 4096, 4
+METRIC = "selected-logprob tokens/s at H=4096,V=151936 bf16; % of roofline; mismatch=0"
+WORKLOAD = "packed training batch T=4096 (8x512), H=4096, V=151936, bf16, 4 vocab shards"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def k1_traffic_record():
+    """Per-launch DRAM bytes of the tile-partials kernel from the committed ncu summary,
+    if it was taken from the library build that is loaded now (else None)."""
+    path = os.path.join(ROOT, "profiles", "tile_partials_packed_T4096.md")
+    try:
+        from invariant_selected_token_gb300 import binding
+        digest = binding.build_fingerprint().split("rev=")[1].split(";")[0]
+        rec = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    rec[k.strip()] = v.strip().strip("`")
+        if rec.get("library_rev") == digest:
+            return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_oracle_sample(hidden_bits, W_bits, targets, rows):
+    """Time the fp64 oracle on the listed rows; returns (seconds, rows)."""
+    from oracle import linear_logprob as oracle
+    t0 = time.perf_counter()
+    oracle.selected_logprob(hidden_bits, W_bits, targets, rows=rows)
+    return time.perf_counter() - t0, (hidden_bits.shape[0] if rows is None else len(rows))
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+    from invariant_selected_token_gb300 import workloads as WL
+    # the same batch as the GPU arm, generated on the CPU when no GPU is used
+    import torch
+    if torch.cuda.is_available():
+        dev = torch.device("cuda:0")
+        W = WL.head_weights(dev)
+        pk = WL.packed(W, dev)
+        hid_bits = WL.bf16_tensor_bits(pk.hidden)
+        tg = pk.targets.cpu().numpy()
+    else:  # same shapes and distributions; uniform targets (they do not change the cost)
+        dev = torch.device("cpu")
+        W = WL.head_weights(dev)
+        hid_bits = WL.bf16_tensor_bits(WL.rms_hidden(T_PACKED, H, dev, 1234))
+        tg = np.random.default_rng(1234).integers(0, V, T_PACKED).astype(np.int32)
+    W_bits = WL.bf16_tensor_bits(W)
+    rows_per_step = 16
+    rng = np.random.default_rng(4321)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(hid_bits, W_bits, tg, rng.choice(T_PACKED, 2, replace=False))
+    times = []
+    for _ in range(args.steps):
+        s, n = cpu_oracle_sample(hid_bits, W_bits, tg, rng.choice(T_PACKED, rows_per_step, replace=False))
+        times.append(s)
+    total = sum(times)
+    value = args.steps * rows_per_step / total
+    cores = os.cpu_count()
+    out = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "T": T_PACKED, "H": H, "V": V, "n_shards": N_SHARDS,
+                      "sample": "%d seeded rows of the batch per step" % rows_per_step},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                            "sample": "%d steps x %d rows of the packed batch, full vocabulary"
+                                      % (args.steps, rows_per_step)},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    import numpy as np
+    import torch
+    from invariant_selected_token_gb300 import binding, workloads as WL
+    from invariant_selected_token_gb300 import build as lib_build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        lib_build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.lib()
+
+    W = WL.head_weights(dev)                       # same weights on every rank
+    pk = WL.packed(W, dev, seed=1234 + 1000 * rank)  # each rank its own batch
+    T = pk.hidden.shape[0]
+    ws = binding.new_workspace(T, V, N_SHARDS, dev)
+    out_lp = torch.empty(T, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev0=None, ev1=None):
+        if ev0 is not None:
+            ev0.record(stream)
+        binding.tile_partials(pk.hidden, W, pk.targets, None, N_SHARDS, ws, status, stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        binding.tile_merge(pk.targets, None, V, N_SHARDS, out_lp, out_lse, ws, status, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status)
+
+    # ---------------- timed region (device-resident inputs)
+    K = args.steps
+    k1_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for k in range(K):
+        step(*k1_ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    ms_total = start.elapsed_time(end)
+    k1_ms = statistics.mean(a.elapsed_time(b) for a, b in k1_ev)
+    binding.raise_on_device_status(status)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / K
+    value = world * T * K / (ms_total / 1000.0)
+
+    # ---------------- end to end through the public call, host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_hidden = pk.hidden.cpu().pin_memory()
+        h_tg = pk.targets.cpu().pin_memory()
+        h_lp = torch.empty(T, dtype=torch.float32).pin_memory()
+        h_lse = torch.empty(T, dtype=torch.float32).pin_memory()
+        d_hidden = torch.empty_like(pk.hidden)
+        d_tg = torch.empty_like(pk.targets)
+
+        def e2e_step():
+            d_hidden.copy_(h_hidden, non_blocking=True)
+            d_tg.copy_(h_tg, non_blocking=True)
+            binding.linear_logprob(d_hidden, W, d_tg, None, N_SHARDS, out_lp, out_lse, ws, status,
+                                   stream)
+            h_lp.copy_(out_lp, non_blocking=True)
+            h_lse.copy_(out_lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * T * K / (e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h_hidden.numel() * 2 + h_tg.numel() * 4),
+               "d2h_bytes_per_step": int(T * 4 * 2)}
+
+    # ---------------- roofline of the dominant kernel (logits GEMM + fused epilogue)
+    peaks = load_peaks()
+    flops = 2.0 * T * H * V
+    achieved_tflops = flops / (k1_ms / 1000.0) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = k1_traffic_record()
+    roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4), "traffic": traffic,
+                "kernel": "k_tile_partials", "kernel_ms": round(k1_ms, 4),
+                "peak_kind": "burst bf16 (%s)" % peaks["source"],
+                "frac_of_sustained": round(achieved_tflops / peaks["bf16_tflops_sustained"], 4)}
+    step_roof_ms = max(flops / (peak * 1e12), (W.numel() * 2 + pk.hidden.numel() * 2)
+                       / (peaks["hbm_gbs"] * 1e9)) * 1000.0
+
+    # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        W_bits = WL.bf16_tensor_bits(W)
+        rows = WL.permutation(T, 4321)[:24]
+        hid_bits = WL.bf16_tensor_bits(pk.hidden[torch.from_numpy(rows).to(dev)])
+        s, n = cpu_oracle_sample(hid_bits, W_bits, pk.targets.cpu().numpy()[rows], None)
+        cpu = {"value": n / s, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "%d rows of the packed batch over the full vocabulary (%.1f s)" % (n, s)}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+               "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": WORKLOAD, "T": T, "H": H, "V": V, "n_shards": N_SHARDS,
+                          "accumulate": "fp32", "l2": "inputs larger than L2 (W = 1.24 GB)",
+                          "parallelism": "dp%d (independent batches)" % world,
+                          "roofline_step_ms": round(step_roof_ms, 4),
+                          "frac_of_step_roofline": round(step_roof_ms / ms_per_step, 4)},
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": 2 * K, "clocks": clk,
+               "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+/*
+ * rlk.h -- C-ABI of the layout-invariant selected-token logprob ("strict-path
+ * linear logprob") for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  For each token t of a batch, with bf16 hidden state
+ * h[t, :] and bf16 output-head weights W[v, :] over the whole vocabulary,
+ *
+ *     lse[t]     = log sum_v exp(h[t] . W[v])
+ *     logprob[t] = h[t] . W[target[t]] - lse[t]
+ *
+ * ("vLLM RL-Kernel v0.1.0: ROCm 上でのビット単位のトレーニング-ロールアウト一貫性",
+ * strict-path boundary table, row "Linear logprob": actual vocabulary range,
+ * target ownership, local reduction, cross-rank LSE merge; the blog on
+ * bitwise consistency with RL-Kernel + vime on AMD, section 3.1: log_softmax
+ * read at the target, whose max and sum reductions fix the last bits).
+ *
+ * The numeric contract "rlk-linlogp-v1" fixes every reduction, merge order,
+ * precision, rounding point and primitive (the same page, section
+ * 数値実行契約), so a token's two results are bit-identical whatever batch it
+ * sits in (1-row decode or a packed batch), whatever its row position, and
+ * however the vocabulary is split into tree-aligned shards:
+ *
+ *   - logits are fp32 tensor-core dot products of bf16 inputs, K ascending in
+ *     steps of 16, one accumulator, never split over K, never rounded to bf16;
+ *   - the vocabulary is cut into tiles of 128 columns; each tile gives
+ *     (m, s) = (max logit, pairwise-tree sum of exp(logit - m)) for its real
+ *     columns (a last, shorter tile simply has fewer columns);
+ *   - tiles merge along one fixed tree (recursive bisection of the tile
+ *     index range, lower half taking the extra tile) with
+ *     merge(L, R) = (hi.m, fma(lo.s, exp(lo.m - hi.m), hi.s)), hi = the
+ *     operand with the larger m, L on a tie;
+ *   - n_shards (1, 2, 4 or 8) shards are the nodes of that tree at depth
+ *     log2(n_shards), so shard records merged in shard order give the same
+ *     bits as the unsharded call;
+ *   - lse = RN(m + log(s)), logprob = RN(target logit - lse);
+ *   - exp and log are the library's own (Cody-Waite + degree-7 Taylor; atanh
+ *     series), not the CUDA math library's.
+ *
+ * Conventions for every call below.
+ *   - Pointers named as device pointers must point to device memory of the
+ *     current CUDA device; the caller owns every buffer.  The library keeps
+ *     no per-call state and allocates no device memory.
+ *   - Calls are asynchronous and stream-ordered on `stream` (NULL = legacy
+ *     default stream); outputs are valid once the stream reaches them.
+ *   - Host-detectable errors are returned before anything is launched.
+ *   - Device-detected errors are OR-ed into *dev_status (a device int32 the
+ *     caller zeroes; may be NULL) as bit (1 << code): RLK_ERR_TARGET_RANGE
+ *     for an active row whose target no shard owns (that row's outputs are
+ *     NaN), RLK_ERR_TIMEOUT if a pipeline wait ran out (outputs undefined;
+ *     the kernel returns instead of hanging).
+ *   - T == 0 is a no-op returning RLK_OK.
+ *   - Inactive rows (active_mask[t] == 0) give out_logprob = out_lse = 0 and
+ *     all-zero partial records; their hidden row and target are never used
+ *     in any other row's result.  active_mask == NULL means all active.
+ *   - Only sm_103 devices are supported; anything else returns
+ *     RLK_ERR_UNSUPPORTED.  There is no fallback path.
+ */
+#ifndef RLK_H_
+#define RLK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st* rlk_stream_t;
+
+typedef enum rlk_status {
+    RLK_OK = 0,
+    RLK_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad shard index */
+    RLK_ERR_UNSUPPORTED = 2,   /* device not sm_103; H % 64 != 0; V > 262144; n_shards not in {1,2,4,8} or > tiles */
+    RLK_ERR_ALIGNMENT = 3,     /* hidden/W not 16-byte aligned, workspace not 256-byte aligned */
+    RLK_ERR_WORKSPACE = 4,     /* workspace smaller than rlk_workspace_size() */
+    RLK_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (launch, device query) */
+    RLK_ERR_TARGET_RANGE = 6,  /* device-detected: active row whose target no shard owns */
+    RLK_ERR_TIMEOUT = 7        /* device-detected: a bounded pipeline wait gave up */
+} rlk_status_t;
+
+/* Per-token record of one vocabulary shard (16 bytes). */
+typedef struct rlk_partial {
+    float m;          /* max logit over the shard's vocabulary range */
+    float s;          /* sum of exp(logit - m) over the range, merged along the tile tree */
+    float tgt;        /* the target's logit if this shard owns the target, else 0 */
+    uint32_t owned;   /* 1 if target lies in [v_begin, v_end) of this shard, else 0 */
+} rlk_partial_t;
+
+#define RLK_VOCAB_TILE 128
+#define RLK_MAX_SHARDS 8
+#define RLK_MAX_VOCAB 262144          /* 2048 tiles */
+#define RLK_K_BLOCK 64                /* H must be a multiple of this */
+
+/* "rlk-linlogp-v1": names the numeric contract above. */
+const char* rlk_contract_id(void);
+
+/* Build fingerprint: source revision, nvcc version, arch and contract flags. */
+const char* rlk_build_fingerprint(void);
+
+/* Human-readable name of a status code. */
+const char* rlk_status_string(int status);
+
+/*
+ * Vocabulary range [*v_begin, *v_end) of shard `shard` of `n_shards`: the
+ * shard-th node at depth log2(n_shards) of the tile tree, in vocabulary ids
+ * (the strict-path table's "actual vocabulary range").  Host only.
+ * Errors: RLK_ERR_INVALID_ARG (null outputs, V < 1, shard out of range),
+ * RLK_ERR_UNSUPPORTED (bad n_shards, V > RLK_MAX_VOCAB).
+ */
+rlk_status_t rlk_shard_range(int64_t V, int n_shards, int shard, int64_t* v_begin, int64_t* v_end);
+
+/*
+ * Bytes of device workspace rlk_linear_logprob needs for (T, V, n_shards);
+ * it also covers rlk_linear_logprob_shard for any shard of that split.
+ * Layout (each part 256-byte aligned): per-tile (m, s) float pairs [T][tiles],
+ * target logits float [T], shard records rlk_partial_t [n_shards][T].
+ * Returns 0 for invalid arguments.
+ */
+size_t rlk_workspace_size(int64_t T, int64_t V, int n_shards);
+
+/*
+ * Full selected-token logprob of T tokens over V vocabulary entries,
+ * vocabulary split into n_shards tree-aligned shards merged in shard order
+ * on this device (the boundary table's local reduction + cross-rank LSE
+ * merge, with the ranks emulated as shards).  The per-shard records are
+ * left in the workspace's record area.
+ *
+ *   hidden       device, bf16 [T][H] row-major, 16-byte aligned
+ *   W            device, bf16 [V][H] row-major (vocabulary rows), 16-byte aligned
+ *   targets      device, int32 [T], global vocabulary ids
+ *   active_mask  device, uint8 [T] (nonzero = active) or NULL
+ *   H            multiple of 64
+ *   V            1 .. RLK_MAX_VOCAB
+ *   n_shards     1, 2, 4 or 8, and at most ceil(V / 128)
+ *   out_logprob  device, float [T];  out_lse  device, float [T]
+ *   workspace    device, 256-byte aligned, >= rlk_workspace_size(T, V, n_shards) bytes
+ *   dev_status   device int32 or NULL (see conventions)
+ */
+rlk_status_t rlk_linear_logprob(const void* hidden, const void* W, const int32_t* targets,
+                                const uint8_t* active_mask, int64_t T, int64_t H, int64_t V,
+                                int n_shards, float* out_logprob, float* out_lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                rlk_stream_t stream);
+
+/*
+ * The part one vocabulary shard (one emulated TP rank) computes: its record
+ * (m, s, tgt, owned) per token from its own weight rows only.
+ *
+ *   W_shard      device, bf16 rows [v_begin, v_end) of the full W (see
+ *                rlk_shard_range), [v_end - v_begin][H] row-major, 16-byte aligned
+ *   targets      global vocabulary ids; ownership is target in [v_begin, v_end)
+ *   V_total      the full vocabulary size (defines the tile tree)
+ *   out_partial  device, rlk_partial_t [T]
+ *   workspace    >= rlk_workspace_size(T, v_end - v_begin, 1) bytes
+ * Other arguments as rlk_linear_logprob.
+ */
+rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
+                                      const int32_t* targets, const uint8_t* active_mask,
+                                      int64_t T, int64_t H, int64_t V_total, int n_shards,
+                                      int shard, rlk_partial_t* out_partial, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      rlk_stream_t stream);
+
+/*
+ * Cross-shard LSE merge in fixed shard order (the boundary table's
+ * "cross-rank LSE merge" and the distributed-aggregation row's fixed rank
+ * reduction order): records merge pairwise (0,1),(2,3),... then pairs of
+ * those; the target logit comes from the one owning shard.
+ *
+ *   partials     HOST array of n_shards DEVICE pointers, each rlk_partial_t [T], shard order
+ *   n_shards     1, 2, 4 or 8
+ *   out_logprob, out_lse  device, float [T]
+ * An active row with no owning shard, or with more than one, gets NaN and
+ * sets RLK_ERR_TARGET_RANGE in *dev_status.
+ */
+rlk_status_t rlk_lse_merge(const rlk_partial_t* const* partials, int n_shards, int64_t T,
+                           const uint8_t* active_mask, float* out_logprob, float* out_lse,
+                           int32_t* dev_status, rlk_stream_t stream);
+
+/*
+ * The two stages of rlk_linear_logprob as separate calls (same kernels,
+ * same bits), so a caller can time or overlap them:
+ *   rlk_tile_partials: logits GEMM + fused per-tile (m, s) and target pick,
+ *                      into the workspace;
+ *   rlk_tile_merge:    tile tree, shard records, final lse/logprob.
+ * Arguments mean what they mean for rlk_linear_logprob; the workspace must
+ * be the same buffer for both calls.
+ */
+rlk_status_t rlk_tile_partials(const void* hidden, const void* W, const int32_t* targets,
+                               const uint8_t* active_mask, int64_t T, int64_t H, int64_t V,
+                               int n_shards, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, rlk_stream_t stream);
+rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, int64_t T,
+                            int64_t V, int n_shards, float* out_logprob, float* out_lse,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            rlk_stream_t stream);
+
+/*
+ * Diagnostic: the fp32 logits [T][V] exactly as the fused path sees them
+ * (same kernel mainloop, the epilogue stores the accumulator instead of
+ * reducing it).  out_logits: device, float [T][V] row-major.  Meant for
+ * tests and for locating a divergence (the blog's advice to dump the
+ * intermediate values, section 5.2).
+ */
+rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
+                              float* out_logits, int32_t* dev_status, rlk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_H_ */

@@ -1,0 +1,257 @@
+"""Python binding of librlk.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this
+module checks tensor dtypes/devices/contiguity, allocates outputs and the
+workspace through torch (device memory and streams are torch's), and passes
+raw pointers to the C-ABI calls declared in include/rlk.h.  If librlk.so is
+missing, every call raises -- there is no other implementation to fall back
+to.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librlk.so")
+
+STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_INVALID_ARG", 2: "RLK_ERR_UNSUPPORTED",
+                3: "RLK_ERR_ALIGNMENT", 4: "RLK_ERR_WORKSPACE", 5: "RLK_ERR_CUDA",
+                6: "RLK_ERR_TARGET_RANGE", 7: "RLK_ERR_TIMEOUT"}
+RLK_ERR_TARGET_RANGE = 6
+RLK_ERR_TIMEOUT = 7
+VOCAB_TILE = 128
+
+EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rlk_shard_range",
+            "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
+            "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits"]
+
+
+class RlkError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__("%s returned %s" % (where, STATUS_NAMES.get(code, str(code))))
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("librlk.so not found at %s; build it with "
+                               "`python -m invariant_selected_token_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        L.rlk_contract_id.restype = ctypes.c_char_p
+        L.rlk_contract_id.argtypes = []
+        L.rlk_build_fingerprint.restype = ctypes.c_char_p
+        L.rlk_build_fingerprint.argtypes = []
+        L.rlk_status_string.restype = ctypes.c_char_p
+        L.rlk_status_string.argtypes = [i32]
+        L.rlk_shard_range.restype = i32
+        L.rlk_shard_range.argtypes = [i64, i32, i32, P, P]
+        L.rlk_workspace_size.restype = sz
+        L.rlk_workspace_size.argtypes = [i64, i64, i32]
+        L.rlk_linear_logprob.restype = i32
+        L.rlk_linear_logprob.argtypes = [P, P, P, P, i64, i64, i64, i32, P, P, P, sz, P, P]
+        L.rlk_linear_logprob_shard.restype = i32
+        L.rlk_linear_logprob_shard.argtypes = [P, P, P, P, i64, i64, i64, i32, i32, P, P, sz, P, P]
+        L.rlk_lse_merge.restype = i32
+        L.rlk_lse_merge.argtypes = [P, i32, i64, P, P, P, P, P]
+        L.rlk_tile_partials.restype = i32
+        L.rlk_tile_partials.argtypes = [P, P, P, P, i64, i64, i64, i32, P, sz, P, P]
+        L.rlk_tile_merge.restype = i32
+        L.rlk_tile_merge.argtypes = [P, P, i64, i64, i32, P, P, P, sz, P, P]
+        L.rlk_debug_logits.restype = i32
+        L.rlk_debug_logits.argtypes = [P, P, i64, i64, i64, P, P, P]
+        _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise RlkError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device, stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t: torch.Tensor, dtype, name: str, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be on a CUDA device" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+
+
+# ----------------------------------------------------------------- host-only calls
+def contract_id() -> str:
+    return lib().rlk_contract_id().decode()
+
+
+def build_fingerprint() -> str:
+    return lib().rlk_build_fingerprint().decode()
+
+
+def shard_range(V: int, n_shards: int, shard: int) -> Tuple[int, int]:
+    b, e = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().rlk_shard_range(V, n_shards, shard, ctypes.byref(b), ctypes.byref(e)),
+           "rlk_shard_range")
+    return b.value, e.value
+
+
+def workspace_size(T: int, V: int, n_shards: int = 1) -> int:
+    n = lib().rlk_workspace_size(T, V, n_shards)
+    if n == 0 and T > 0:
+        raise RlkError(1, "rlk_workspace_size")
+    return int(n)
+
+
+def new_workspace(T: int, V: int, n_shards: int, device) -> torch.Tensor:
+    return torch.empty(max(256, workspace_size(T, V, n_shards)), dtype=torch.uint8, device=device)
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def raise_on_device_status(status: torch.Tensor):
+    """Synchronise on the status word and raise for the first error bit set."""
+    word = int(status.item())
+    for code in sorted(STATUS_NAMES):
+        if code and word & (1 << code):
+            raise RlkError(code, "device status 0x%x" % word)
+
+
+# ----------------------------------------------------------------- device calls
+def linear_logprob(hidden: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
+                   active: Optional[torch.Tensor] = None, n_shards: int = 1,
+                   out_logprob: Optional[torch.Tensor] = None,
+                   out_lse: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None
+                   ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(logprob [T], lse [T]) fp32 for bf16 hidden [T,H], W [V,H], int32 targets [T]."""
+    dev = hidden.device
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W, torch.bfloat16, "W", dev, ndim=2)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    if active is not None:
+        _require(active, torch.uint8, "active", dev, ndim=1)
+    T, H = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != H or targets.shape[0] != T or (active is not None and active.shape[0] != T):
+        raise ValueError("shape mismatch")
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, V, n_shards, dev)
+    _check(lib().rlk_linear_logprob(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H, V,
+                                    n_shards, _ptr(out_logprob), _ptr(out_lse), _ptr(workspace),
+                                    workspace.numel(), _ptr(status), _stream(dev, stream)),
+           "rlk_linear_logprob")
+    return out_logprob, out_lse
+
+
+def tile_partials(hidden, W, targets, active, n_shards, workspace, status=None, stream=None):
+    dev = hidden.device
+    T, H = hidden.shape
+    _check(lib().rlk_tile_partials(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H,
+                                   W.shape[0], n_shards, _ptr(workspace), workspace.numel(),
+                                   _ptr(status), _stream(dev, stream)), "rlk_tile_partials")
+
+
+def tile_merge(targets, active, V, n_shards, out_logprob, out_lse, workspace, status=None,
+               stream=None):
+    dev = targets.device
+    T = targets.shape[0]
+    _check(lib().rlk_tile_merge(_ptr(targets), _ptr(active), T, V, n_shards, _ptr(out_logprob),
+                                _ptr(out_lse), _ptr(workspace), workspace.numel(), _ptr(status),
+                                _stream(dev, stream)), "rlk_tile_merge")
+
+
+def workspace_records(workspace: torch.Tensor, T: int, V: int, n_shards: int) -> torch.Tensor:
+    """View of the shard records rlk_linear_logprob leaves in its workspace: int32 [n_shards, T, 4]."""
+    nt = (V + VOCAB_TILE - 1) // VOCAB_TILE
+    a256 = lambda x: (x + 255) & ~255  # noqa: E731
+    off = a256(T * nt * 8) + a256(T * 4)
+    return workspace[off:off + n_shards * T * 16].view(torch.int32).view(n_shards, T, 4)
+
+
+def linear_logprob_shard(hidden, W_shard, targets, active, V_total: int, n_shards: int,
+                         shard: int, out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, status=None, stream=None
+                         ) -> torch.Tensor:
+    """One shard's records as int32 [T, 4] (m, s, tgt as fp32 bits; owned as uint32)."""
+    dev = hidden.device
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W_shard, torch.bfloat16, "W_shard", dev, ndim=2)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    T, H = hidden.shape
+    vb, ve = shard_range(V_total, n_shards, shard)
+    if W_shard.shape[0] != ve - vb:
+        raise ValueError("W_shard has %d rows, shard %d covers %d" % (W_shard.shape[0], shard, ve - vb))
+    if out is None:
+        out = torch.empty((T, 4), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, ve - vb, 1, dev)
+    _check(lib().rlk_linear_logprob_shard(_ptr(hidden), _ptr(W_shard), _ptr(targets),
+                                          _ptr(active), T, H, V_total, n_shards, shard, _ptr(out),
+                                          _ptr(workspace), workspace.numel(), _ptr(status),
+                                          _stream(dev, stream)), "rlk_linear_logprob_shard")
+    return out
+
+
+def lse_merge(partials: Sequence[torch.Tensor], active=None, out_logprob=None, out_lse=None,
+              status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    n = len(partials)
+    dev = partials[0].device
+    T = partials[0].shape[0]
+    for p in partials:
+        _require(p, torch.int32, "partial", dev, ndim=2)
+    arr = (ctypes.c_void_p * n)(*[p.data_ptr() for p in partials])
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    _check(lib().rlk_lse_merge(ctypes.cast(arr, ctypes.c_void_p), n, T, _ptr(active),
+                               _ptr(out_logprob), _ptr(out_lse), _ptr(status),
+                               _stream(dev, stream)), "rlk_lse_merge")
+    return out_logprob, out_lse
+
+
+def debug_logits(hidden: torch.Tensor, W: torch.Tensor, status=None, stream=None) -> torch.Tensor:
+    dev = hidden.device
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W, torch.bfloat16, "W", dev, ndim=2)
+    T, H = hidden.shape
+    V = W.shape[0]
+    out = torch.empty((T, V), dtype=torch.float32, device=dev)
+    _check(lib().rlk_debug_logits(_ptr(hidden), _ptr(W), T, H, V, _ptr(out), _ptr(status),
+                                  _stream(dev, stream)), "rlk_debug_logits")
+    return out
+
+
+def shard_ranges(V: int, n_shards: int) -> List[Tuple[int, int]]:
+    return [shard_range(V, n_shards, r) for r in range(n_shards)]

@@ -1,0 +1,407 @@
+// Host side of the C-ABI (include/rlk.h): argument checks, the canonical
+// tile tree on the host, workspace layout, TMA descriptor encoding and kernel
+// dispatch.  Strict mode only: anything unsupported is refused with a
+// status code, nothing falls back to another path ("vLLM RL-Kernel v0.1.0",
+// strict path; the vime ablation-matrix issue, "strict: unsupported 时 fail
+// closed").
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "rlk_internal.h"
+
+#ifndef RLK_GIT_REV
+#define RLK_GIT_REV "unknown"
+#endif
+#ifndef RLK_NVCC_VERSION
+#define RLK_NVCC_VERSION "unknown"
+#endif
+
+namespace {
+
+using rlk::kTileM;
+using rlk::kTileN;
+using rlk::kVocabTile;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sm_count = 0;
+    int cc = 0;  // 10 * major + minor
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int64_t n_tiles_of(int64_t V) { return (V + kVocabTile - 1) / kVocabTile; }
+
+int log2_exact(int n) {
+    int d = 0;
+    while ((1 << d) < n) ++d;
+    return (1 << d) == n ? d : -1;
+}
+
+int tree_depth(int64_t n_tiles) {
+    int d = 0;
+    while ((int64_t(1) << d) < n_tiles) ++d;
+    return d;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Tile range [first, first + count) of node `index` at depth `depth` of the
+// recursive bisection of [0, n_tiles) (the lower half takes the extra tile).
+bool tree_node(int64_t n_tiles, int depth, int index, int64_t* first, int64_t* count) {
+    int64_t f = 0, k = n_tiles;
+    for (int b = depth - 1; b >= 0; --b) {
+        if (k < 2) return false;
+        const int64_t left = (k + 1) / 2;
+        if ((index >> b) & 1) {
+            f += left;
+            k -= left;
+        } else {
+            k = left;
+        }
+    }
+    *first = f;
+    *count = k;
+    return k >= 1;
+}
+
+struct Layout {
+    size_t partials, tgt, records, total;
+};
+
+Layout layout_of(int64_t T, int64_t V, int n_shards) {
+    Layout l;
+    l.partials = 0;
+    l.tgt = align256(size_t(T) * size_t(n_tiles_of(V)) * sizeof(float2));
+    l.records = l.tgt + align256(size_t(T) * sizeof(float));
+    l.total = l.records + align256(size_t(T) * size_t(n_shards) * sizeof(rlk_partial_t));
+    return l;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+rlk_status_t shard_check(int64_t V, int n_shards) {
+    if (V < 1) return RLK_ERR_INVALID_ARG;
+    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
+    const int d = log2_exact(n_shards);
+    if (n_shards < 1 || n_shards > RLK_MAX_SHARDS || d < 0) return RLK_ERR_UNSUPPORTED;
+    if (int64_t(n_shards) > n_tiles_of(V)) return RLK_ERR_UNSUPPORTED;
+    return RLK_OK;
+}
+
+// Device of the calling thread: must be sm_103.  RLK_TEST_DEVICE_CC
+// (e.g. "100") makes the check see another compute capability, so the
+// refusal path can be exercised on real hardware without launching anything.
+rlk_status_t device_check(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RLK_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RLK_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return RLK_ERR_CUDA;
+        st.cc = major * 10 + minor;
+        st.sm_count = sms;
+        if (st.cc == 103) {
+            if (rlk::prepare_tile_partials_kernels() != cudaSuccess) return RLK_ERR_CUDA;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return RLK_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        st.ready = true;
+    }
+    int cc = st.cc;
+    if (const char* fake = std::getenv("RLK_TEST_DEVICE_CC")) cc = std::atoi(fake);
+    if (cc != 103) return RLK_ERR_UNSUPPORTED;
+    *out = &st;
+    return RLK_OK;
+}
+
+// bf16 [rows][inner] row-major, boxes of 64 (inner) x box_rows, 128-byte swizzle.
+rlk_status_t encode_bf16_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                             uint32_t box_rows) {
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(inner) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(rlk::kBlockK), box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t* targets,
+                               const uint8_t* active, int64_t T, int64_t H, int64_t V_local,
+                               int64_t v_offset, float2* partials, float* tgt, float* dbg,
+                               int32_t* status, cudaStream_t stream, const DeviceState* dev) {
+    CUtensorMap map_h, map_w;
+    rlk_status_t s = encode_bf16_map(&map_h, hidden, H, T, kTileM);
+    if (s != RLK_OK) return s;
+    s = encode_bf16_map(&map_w, W, H, V_local, kTileN);
+    if (s != RLK_OK) return s;
+    rlk::TilePartialsArgs a;
+    a.targets = targets;
+    a.active = active;
+    a.partials = partials;
+    a.tgt_logit = tgt;
+    a.dbg_logits = dbg;
+    a.status = status;
+    a.v_offset = v_offset;
+    a.T = int(T);
+    a.V_local = int(V_local);
+    a.n_tiles = int(n_tiles_of(V_local));
+    a.k_blocks = int(H / rlk::kBlockK);
+    return rlk::launch_tile_partials(map_h, map_w, a, dbg != nullptr, dev->sm_count, stream) ==
+                   cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
+}
+
+rlk_status_t common_checks(const void* hidden, const void* W, const int32_t* targets, int64_t T,
+                           int64_t H) {
+    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    if (T > 0 && (!hidden || !W || !targets)) return RLK_ERR_INVALID_ARG;
+    if (H < rlk::kBlockK || H % rlk::kBlockK != 0 || H > (int64_t(1) << 20)) return RLK_ERR_UNSUPPORTED;
+    if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(targets, 4)) return RLK_ERR_ALIGNMENT;
+    return RLK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rlk_contract_id(void) { return "rlk-linlogp-v1"; }
+
+const char* rlk_build_fingerprint(void) {
+    return "rlk-linlogp-v1; rev=" RLK_GIT_REV "; nvcc=" RLK_NVCC_VERSION
+           "; arch=sm_103a; flags=-O3 -ftz=false -prec-div=true -prec-sqrt=true -fmad=false";
+}
+
+const char* rlk_status_string(int status) {
+    switch (status) {
+        case RLK_OK: return "RLK_OK";
+        case RLK_ERR_INVALID_ARG: return "RLK_ERR_INVALID_ARG";
+        case RLK_ERR_UNSUPPORTED: return "RLK_ERR_UNSUPPORTED";
+        case RLK_ERR_ALIGNMENT: return "RLK_ERR_ALIGNMENT";
+        case RLK_ERR_WORKSPACE: return "RLK_ERR_WORKSPACE";
+        case RLK_ERR_CUDA: return "RLK_ERR_CUDA";
+        case RLK_ERR_TARGET_RANGE: return "RLK_ERR_TARGET_RANGE";
+        case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT";
+        default: return "RLK_ERR_UNKNOWN";
+    }
+}
+
+rlk_status_t rlk_shard_range(int64_t V, int n_shards, int shard, int64_t* v_begin,
+                             int64_t* v_end) {
+    if (!v_begin || !v_end) return RLK_ERR_INVALID_ARG;
+    const rlk_status_t s = shard_check(V, n_shards);
+    if (s != RLK_OK) return s;
+    if (shard < 0 || shard >= n_shards) return RLK_ERR_INVALID_ARG;
+    int64_t first = 0, count = 0;
+    if (!tree_node(n_tiles_of(V), log2_exact(n_shards), shard, &first, &count))
+        return RLK_ERR_UNSUPPORTED;
+    *v_begin = first * kVocabTile;
+    const int64_t e = (first + count) * kVocabTile;
+    *v_end = e < V ? e : V;
+    return RLK_OK;
+}
+
+size_t rlk_workspace_size(int64_t T, int64_t V, int n_shards) {
+    if (T < 0 || shard_check(V, n_shards) != RLK_OK) return 0;
+    return layout_of(T, V, n_shards).total;
+}
+
+rlk_status_t rlk_tile_partials(const void* hidden, const void* W, const int32_t* targets,
+                               const uint8_t* active_mask, int64_t T, int64_t H, int64_t V,
+                               int n_shards, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_status, rlk_stream_t stream) {
+    rlk_status_t s = common_checks(hidden, W, targets, T, H);
+    if (s != RLK_OK) return s;
+    if ((s = shard_check(V, n_shards)) != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!workspace) return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return RLK_ERR_ALIGNMENT;
+    const Layout l = layout_of(T, V, n_shards);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    return run_tile_partials(hidden, W, targets, active_mask, T, H, V, 0,
+                             reinterpret_cast<float2*>(ws + l.partials),
+                             reinterpret_cast<float*>(ws + l.tgt), nullptr, dev_status,
+                             reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, int64_t T,
+                            int64_t V, int n_shards, float* out_logprob, float* out_lse,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            rlk_stream_t stream) {
+    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    rlk_status_t s = shard_check(V, n_shards);
+    if (s != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!targets || !out_logprob || !out_lse || !workspace) return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(targets, 4) || !aligned(out_logprob, 4) ||
+        !aligned(out_lse, 4))
+        return RLK_ERR_ALIGNMENT;
+    const Layout l = layout_of(T, V, n_shards);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int64_t nt = n_tiles_of(V);
+    rlk::TileTreeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.partials = reinterpret_cast<const float2*>(ws + l.partials);
+    a.ld = nt;
+    a.tgt_logit = reinterpret_cast<const float*>(ws + l.tgt);
+    a.targets = targets;
+    a.active = active_mask;
+    a.status = dev_status;
+    a.T = int(T);
+    a.n_tiles = int(nt);
+    a.depth = tree_depth(nt);
+    a.shard_depth = log2_exact(n_shards);
+    a.n_shards = n_shards;
+    a.shard_mode = 0;
+    for (int r = 0; r < n_shards; ++r) {
+        int64_t b = 0, e = 0;
+        rlk_shard_range(V, n_shards, r, &b, &e);
+        a.shard_vbegin[r] = b;
+        a.shard_vbegin[r + 1] = e;
+    }
+    a.V_total = V;
+    a.out_logprob = out_logprob;
+    a.out_lse = out_lse;
+    a.records = reinterpret_cast<rlk_partial_t*>(ws + l.records);
+    return rlk::launch_tile_tree(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
+}
+
+rlk_status_t rlk_linear_logprob(const void* hidden, const void* W, const int32_t* targets,
+                                const uint8_t* active_mask, int64_t T, int64_t H, int64_t V,
+                                int n_shards, float* out_logprob, float* out_lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                rlk_stream_t stream) {
+    if (T > 0 && (!out_logprob || !out_lse)) return RLK_ERR_INVALID_ARG;
+    rlk_status_t s = rlk_tile_partials(hidden, W, targets, active_mask, T, H, V, n_shards,
+                                       workspace, workspace_bytes, dev_status, stream);
+    if (s != RLK_OK) return s;
+    return rlk_tile_merge(targets, active_mask, T, V, n_shards, out_logprob, out_lse, workspace,
+                          workspace_bytes, dev_status, stream);
+}
+
+rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
+                                      const int32_t* targets, const uint8_t* active_mask,
+                                      int64_t T, int64_t H, int64_t V_total, int n_shards,
+                                      int shard, rlk_partial_t* out_partial, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      rlk_stream_t stream) {
+    rlk_status_t s = common_checks(hidden, W_shard, targets, T, H);
+    if (s != RLK_OK) return s;
+    int64_t vb = 0, ve = 0;
+    if ((s = rlk_shard_range(V_total, n_shards, shard, &vb, &ve)) != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!out_partial || !workspace) return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(out_partial, 16)) return RLK_ERR_ALIGNMENT;
+    const int64_t V_local = ve - vb;
+    const Layout l = layout_of(T, V_local, 1);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    s = run_tile_partials(hidden, W_shard, targets, active_mask, T, H, V_local, vb,
+                          reinterpret_cast<float2*>(ws + l.partials),
+                          reinterpret_cast<float*>(ws + l.tgt), nullptr, dev_status, st, dev);
+    if (s != RLK_OK) return s;
+    const int64_t nt = n_tiles_of(V_local);
+    rlk::TileTreeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.partials = reinterpret_cast<const float2*>(ws + l.partials);
+    a.ld = nt;
+    a.tgt_logit = reinterpret_cast<const float*>(ws + l.tgt);
+    a.targets = targets;
+    a.active = active_mask;
+    a.status = dev_status;
+    a.T = int(T);
+    a.n_tiles = int(nt);
+    a.depth = tree_depth(nt);
+    a.shard_depth = 0;
+    a.n_shards = 1;
+    a.shard_mode = 1;
+    a.own_begin = vb;
+    a.own_end = ve;
+    a.V_total = V_total;
+    a.records = out_partial;
+    return rlk::launch_tile_tree(a, st) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status_t rlk_lse_merge(const rlk_partial_t* const* partials, int n_shards, int64_t T,
+                           const uint8_t* active_mask, float* out_logprob, float* out_lse,
+                           int32_t* dev_status, rlk_stream_t stream) {
+    if (T < 0 || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (n_shards < 1 || n_shards > RLK_MAX_SHARDS || log2_exact(n_shards) < 0)
+        return RLK_ERR_UNSUPPORTED;
+    if (T == 0) return RLK_OK;
+    if (!partials || !out_logprob || !out_lse) return RLK_ERR_INVALID_ARG;
+    rlk::ShardMergeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    for (int r = 0; r < n_shards; ++r) {
+        if (!partials[r]) return RLK_ERR_INVALID_ARG;
+        if (!aligned(partials[r], 16)) return RLK_ERR_ALIGNMENT;
+        a.parts[r] = partials[r];
+    }
+    DeviceState* dev = nullptr;
+    rlk_status_t s = device_check(&dev);
+    if (s != RLK_OK) return s;
+    a.n_shards = n_shards;
+    a.T = int(T);
+    a.active = active_mask;
+    a.out_logprob = out_logprob;
+    a.out_lse = out_lse;
+    a.status = dev_status;
+    return rlk::launch_shard_merge(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
+}
+
+rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
+                              float* out_logits, int32_t* dev_status, rlk_stream_t stream) {
+    // targets are not read in this mode; pass W as a stand-in non-null pointer for the checks
+    rlk_status_t s = common_checks(hidden, W, reinterpret_cast<const int32_t*>(W), T, H);
+    if (s != RLK_OK) return s;
+    if (V < 1) return RLK_ERR_INVALID_ARG;
+    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
+    if (T == 0) return RLK_OK;
+    if (!out_logits) return RLK_ERR_INVALID_ARG;
+    if (!aligned(out_logits, 4)) return RLK_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    return run_tile_partials(hidden, W, nullptr, nullptr, T, H, V, 0, nullptr, nullptr, out_logits,
+                             dev_status, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+}  // extern "C"

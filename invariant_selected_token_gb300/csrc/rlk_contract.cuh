@@ -1,0 +1,105 @@
+// Device side of the numeric contract "rlk-linlogp-v1": the library's own
+// exp and log, and the (max, sum-exp) merge operator.
+//
+// The pages require the primitives to be fixed, not which ones ("vLLM
+// RL-Kernel v0.1.0: ROCm 上でのビット単位のトレーニング-ロールアウト一貫性",
+// section 数値実行契約, item 6: exp, log, ... FMA; the Chinese report "ROCm上
+// 实现训练与推理logprob逐位对齐", section 技术路径, "数学原语").  Vendor exp/log
+// may differ in the last place between implementations, so the contract
+// defines its own from textbook methods and writes every operation with an
+// explicit IEEE round-to-nearest intrinsic: no compiler contraction, no
+// fast-math reassociation can change a bit.
+#pragma once
+
+#include <cstdint>
+#include <math_constants.h>
+
+namespace rlk {
+
+// exp(x) for x <= 0 (the only arguments the contract forms: logit - max and
+// max differences).  Cody-Waite reduction x = n ln2 + r, |r| <= ln2/2, with
+// n the nearest integer to x log2(e) (taken from the rounding of an fma
+// against 1.5 * 2^23), r in two fma steps against a two-part ln 2; e^r by its
+// degree-7 Taylor polynomial (coefficients 1/k! rounded to fp32) in Horner
+// form; then an exact scaling by 2^n.  Arguments below -86 give +0, which
+// keeps 2^n a normal number; their true value is below 2^-124 and vanishes
+// next to the tile maximum's exp(0) = 1 in every sum the contract forms.
+// Accuracy: under 1 ulp over [-86, 0] (checked exhaustively on the CPU).
+__device__ __forceinline__ float contract_exp(float x) {
+    const float kLog2e = 0x1.715476p+0f;
+    const float kShift = 0x1.8p+23f;
+    const float kLn2Hi = 0x1.62e430p-1f;
+    const float kLn2Lo = -0x1.05c610p-29f;
+    const float t = __fmaf_rn(x, kLog2e, kShift);
+    const float n = __fsub_rn(t, kShift);
+    const int ni = __float_as_int(t) - __float_as_int(kShift);
+    float r = __fmaf_rn(-n, kLn2Hi, x);
+    r = __fmaf_rn(-n, kLn2Lo, r);
+    float p = 0x1.a01a02p-13f;             // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);             // 1/2!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/1!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/0!
+    const float y = __fmul_rn(p, __int_as_float((ni + 127) << 23));
+    return (x < -86.0f) ? 0.0f : y;
+}
+
+// log(s) for positive normal s (the contract only takes the log of a root
+// sum, which lies in [1, 2^21]).  s = 2^e f with f in [sqrt(1/2), sqrt(2)];
+// log f = 2 atanh(u), u = (f - 1)/(f + 1), by the odd series through u^11;
+// log s = e ln2 + log f with the same two-part ln 2.  Accuracy: within 2 ulp
+// on [1, 2^21] (checked exhaustively on the CPU).
+__device__ __forceinline__ float contract_log(float s) {
+    const float kLn2Hi = 0x1.62e430p-1f;
+    const float kLn2Lo = -0x1.05c610p-29f;
+    const int bits = __float_as_int(s);
+    int e = (bits >> 23) - 127;
+    float f = __int_as_float((bits & 0x007FFFFF) | 0x3F800000);
+    if (f > 0x1.6a09e6p+0f) {  // sqrt(2) rounded to fp32
+        f = __fmul_rn(f, 0.5f);
+        e += 1;
+    }
+    const float u = __fdiv_rn(__fsub_rn(f, 1.0f), __fadd_rn(f, 1.0f));
+    const float u2 = __fmul_rn(u, u);
+    float p = 0x1.745d18p-3f;             // 2/11
+    p = __fmaf_rn(p, u2, 0x1.c71c72p-3f);  // 2/9
+    p = __fmaf_rn(p, u2, 0x1.24924ap-2f);  // 2/7
+    p = __fmaf_rn(p, u2, 0x1.99999ap-2f);  // 2/5
+    p = __fmaf_rn(p, u2, 0x1.555556p-1f);  // 2/3
+    const float logf_ = __fmaf_rn(p, __fmul_rn(u, u2), __fmul_rn(2.0f, u));
+    const float ef = __int2float_rn(e);
+    return __fmaf_rn(ef, kLn2Hi, __fmaf_rn(ef, kLn2Lo, logf_));
+}
+
+// A (max, sum of exp(x - max)) pair.
+struct MaxSum {
+    float m;
+    float s;
+};
+
+// The contract's merge: the operand with the larger max is kept ("hi"; the
+// left operand on a tie), the other's sum is scaled by exp(lo.m - hi.m) and
+// added with one fused rounding.  On a tie exp(0) = 1 exactly, so the result
+// is RN(s_left + s_right) whichever side is left.
+//
+// Padding slots of the GPU's power-of-two tree carry m = -inf, s = 0; the
+// contract's own tree never forms them, and a padding operand must pass the
+// other one through unchanged, which the final select guarantees (it also
+// keeps -inf - -inf from producing a NaN).
+__device__ __forceinline__ MaxSum contract_merge(MaxSum left, MaxSum right) {
+    const bool right_hi = right.m > left.m;
+    const float mh = right_hi ? right.m : left.m;
+    const float sh = right_hi ? right.s : left.s;
+    const float ml = right_hi ? left.m : right.m;
+    const float sl = right_hi ? left.s : right.s;
+    const float scaled = __fmaf_rn(sl, contract_exp(__fsub_rn(ml, mh)), sh);
+    MaxSum out;
+    out.m = mh;
+    out.s = (ml == -CUDART_INF_F) ? sh : scaled;
+    return out;
+}
+
+}  // namespace rlk

@@ -1,0 +1,76 @@
+// Internal launch interface between the host dispatcher (rlk_api.cu) and the
+// kernels (rlk_logits.cu: logits GEMM + fused tile epilogue; rlk_merge.cu:
+// tile tree, shard records, finalize, cross-shard merge).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/rlk.h"
+
+namespace rlk {
+
+constexpr int kTileM = 128;          // token rows per MMA tile
+constexpr int kTileN = 256;          // vocabulary rows per MMA tile (two contract tiles)
+constexpr int kVocabTile = RLK_VOCAB_TILE;
+constexpr int kBlockK = RLK_K_BLOCK; // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kMaxTreeDepth = 11;    // 2048 tiles
+
+struct TilePartialsArgs {
+    const int32_t* targets;   // [T] global vocabulary ids
+    const uint8_t* active;    // [T] or nullptr
+    float2* partials;         // [T][n_tiles] (m, s); unused in debug mode
+    float* tgt_logit;         // [T] target logit, written by the owning tile
+    float* dbg_logits;        // [T][V_local], debug mode only
+    int32_t* status;          // device status bits or nullptr
+    int64_t v_offset;         // global vocabulary id of W row 0
+    int T;
+    int V_local;              // rows of W this launch covers
+    int n_tiles;              // ceil(V_local / 128): row stride of partials
+    int k_blocks;             // H / 64
+};
+
+// hidden map: bf16 [T][H], box 64 x 128; weight map: bf16 [V_local][H], box 64 x 256.
+cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
+                                 const TilePartialsArgs& a, bool debug_logits, int num_sms,
+                                 cudaStream_t stream);
+int tile_partials_smem_bytes();
+cudaError_t prepare_tile_partials_kernels();
+
+struct TileTreeArgs {
+    const float2* partials;   // [T][ld]
+    int64_t ld;
+    const float* tgt_logit;   // [T]
+    const int32_t* targets;   // [T]
+    const uint8_t* active;    // [T] or nullptr
+    int32_t* status;
+    int T;
+    int n_tiles;              // leaves of this tree
+    int depth;                // ceil(log2(n_tiles))
+    int shard_depth;          // log2(n_shards) (full mode); 0 in shard mode
+    int n_shards;
+    int shard_mode;           // 0: full tree -> records + outputs; 1: one shard's record
+    int64_t shard_vbegin[RLK_MAX_SHARDS + 1];  // vocabulary boundaries (full mode)
+    int64_t own_begin, own_end;                 // ownership range (shard mode)
+    int64_t V_total;
+    float* out_logprob;       // [T] (full mode)
+    float* out_lse;           // [T] (full mode)
+    rlk_partial_t* records;   // full: [n_shards][T]; shard: [T]
+};
+
+cudaError_t launch_tile_tree(const TileTreeArgs& a, cudaStream_t stream);
+
+struct ShardMergeArgs {
+    const rlk_partial_t* parts[RLK_MAX_SHARDS];
+    int n_shards;
+    int T;
+    const uint8_t* active;
+    float* out_logprob;
+    float* out_lse;
+    int32_t* status;
+};
+
+cudaError_t launch_shard_merge(const ShardMergeArgs& a, cudaStream_t stream);
+
+}  // namespace rlk

@@ -1,0 +1,310 @@
+// Logits GEMM with the fused per-tile epilogue (the "local reduction" and
+// "target ownership" of the strict-path table's Linear-logprob row, in
+// "vLLM RL-Kernel v0.1.0: ROCm 上でのビット単位のトレーニング-ロールアウト一貫性").
+//
+// One persistent CTA per SM walks output tiles of 128 tokens x 256
+// vocabulary rows, vocabulary-major (all token tiles of one W slice run
+// side by side, so each 2 MB slice of W is read from HBM once and shared
+// through L2).  Warp roles:
+//   warp 0      TMA producer: 4-stage ring of (hidden 128x64, W 256x64) bf16
+//               boxes, 128-byte swizzled;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16, M=128,
+//               N=256, K=16, cta_group::1, fp32 accumulator in TMEM, K in
+//               ascending order, the first step overwriting; two
+//               accumulators (2 x 256 TMEM columns) so the epilogue of tile
+//               i overlaps the mainloop of tile i+1;
+//   warps 2-5   epilogue: one thread per token row (TMEM lane), 128 columns
+//               per contract tile read with tcgen05.ld, reduced in registers
+//               to (max, pairwise-tree sum of exp(logit - max)) and the
+//               target's logit picked if the tile owns it.  The [T, V]
+//               logits never reach HBM.
+//
+// Invariance: every logit comes from the same instruction sequence whatever
+// T, the row position or the launch shape, so the per-tile values depend on
+// the token and the tile only.  There is no split over K on any path.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "rlk_contract.cuh"
+#include "rlk_internal.h"
+#include "rlk_ptx.cuh"
+
+namespace rlk {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kStageBytesA = kTileM * kBlockK * 2;  // 16 KB
+constexpr uint32_t kStageBytesB = kTileN * kBlockK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 512;                      // two 256-column accumulators
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kTileN);
+constexpr int kSmemBytes = kStages * (kStageBytesA + kStageBytesB) + 1024 /*alignment slack*/
+                           + 256 /*barriers, TMEM address, abort flag*/;
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+    if (status) atomicOr(status, 1 << code);
+}
+
+// Reduce one 128-column contract tile held in registers (v[c] = logit of
+// column c; columns at or beyond ncols are padding) to (max, sum).
+// The sum is the contract's 128-slot pairwise tree: (0+1), (2+3), ..., then
+// pairs of those, seven levels.  A padding column is set to -inf, whose exp
+// is +0, and x + 0 = x exactly for the non-negative terms here, so padding
+// slots pass their partner through unchanged, as the contract requires.
+__device__ __forceinline__ MaxSum reduce_tile(float (&v)[kVocabTile], int ncols) {
+    if (ncols < kVocabTile) {
+#pragma unroll
+        for (int c = 0; c < kVocabTile; ++c)
+            if (c >= ncols) v[c] = -CUDART_INF_F;
+    }
+    // max is exact, so its evaluation order is free; four chains for ILP
+    float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+#pragma unroll
+    for (int c = 4; c < kVocabTile; c += 4) {
+        m0 = fmaxf(m0, v[c]);
+        m1 = fmaxf(m1, v[c + 1]);
+        m2 = fmaxf(m2, v[c + 2]);
+        m3 = fmaxf(m3, v[c + 3]);
+    }
+    const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+    for (int c = 0; c < kVocabTile; ++c) v[c] = contract_exp(__fsub_rn(v[c], m));
+#pragma unroll
+    for (int w = kVocabTile / 2; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
+    }
+    MaxSum r;
+    r.m = m;
+    r.s = v[0];
+    return r;
+}
+
+template <bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
+                    const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kStageBytesA;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageBytesB);
+    uint64_t* empty = full + kStages;
+    uint64_t* acc_full = empty + kStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (a.T + kTileM - 1) / kTileM;
+    const int num_n = (a.V_local + kTileN - 1) / kTileN;
+    const int total = num_m * num_n;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], 4 * 32);
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tensormap(&map_hidden);
+        ptx::prefetch_tensormap(&map_w);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            uint32_t stage = 0, phase = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+                const int n_blk = tile / num_m;
+                const int m_blk = tile - n_blk * num_m;
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        *abort_flag = 1;
+                        report(a.status, RLK_ERR_TIMEOUT);
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[stage], kStageBytesA + kStageBytesB);
+                    ptx::tma_load_2d(sA + stage * kStageBytesA, &map_hidden, &full[stage],
+                                     kb * kBlockK, m_blk * kTileM);
+                    ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
+                                     kb * kBlockK, n_blk * kTileN);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+                if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    report(a.status, RLK_ERR_TIMEOUT);
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * kTileN;
+                bool ok = true;
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a0 = ptx::smem_addr(sA + stage * kStageBytesA);
+                    const uint32_t b0 = ptx::smem_addr(sB + stage * kStageBytesB);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle row
+                        ptx::mma_bf16(d_tmem, ptx::smem_desc_k_sw128(a0 + kk * 32),
+                                      ptx::smem_desc_k_sw128(b0 + kk * 32), kIdesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    report(a.status, RLK_ERR_TIMEOUT);
+                    break;
+                }
+                ptx::mma_commit(&acc_full[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5; TMEM lane quadrant = warp % 4)
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const int n_blk = tile / num_m;
+            const int m_blk = tile - n_blk * num_m;
+            if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) {
+                *abort_flag = 1;
+                report(a.status, RLK_ERR_TIMEOUT);
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            const int t = m_blk * kTileM + row;
+            bool valid = t < a.T;
+            if (valid && a.active) valid = a.active[t] != 0;
+            const int64_t tg_local =
+                (!kDebug && valid) ? static_cast<int64_t>(a.targets[t]) - a.v_offset : -1;
+            if (__any_sync(0xffffffffu, kDebug ? (t < a.T) : valid)) {
+#pragma unroll 1
+                for (int sub = 0; sub < kTileN / kVocabTile; ++sub) {
+                    const int j = n_blk * (kTileN / kVocabTile) + sub;
+                    const int c0 = j * kVocabTile;
+                    if (c0 >= a.V_local) break;
+                    const int ncols = min(kVocabTile, a.V_local - c0);
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                           acc * kTileN + sub * kVocabTile;
+                    float v[kVocabTile];
+                    __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+#pragma unroll
+                    for (int q = 0; q < kVocabTile / 32; ++q) {
+                        float part[32];
+                        ptx::tmem_load_32cols(taddr + q * 32, part);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[q * 32 + i] = part[i];
+                    }
+                    if (kDebug) {
+                        if (t < a.T) {
+                            float* dst = a.dbg_logits + static_cast<int64_t>(t) * a.V_local + c0;
+                            for (int c = 0; c < ncols; ++c) dst[c] = v[c];
+                        }
+                        continue;
+                    }
+                    const int64_t tl = tg_local - c0;
+                    const bool own = valid && tl >= 0 && tl < ncols;
+                    if (__any_sync(0xffffffffu, own)) {
+                        const int ti = own ? static_cast<int>(tl) : -1;
+                        float tv = 0.0f;
+#pragma unroll
+                        for (int c = 0; c < kVocabTile; ++c) tv = (c == ti) ? v[c] : tv;
+                        if (own) a.tgt_logit[t] = tv;
+                    }
+                    const MaxSum r = reduce_tile(v, ncols);
+                    if (valid)
+                        a.partials[static_cast<int64_t>(t) * a.n_tiles + j] = make_float2(r.m, r.s);
+                }
+            }
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(&acc_empty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        // a wait gave up: let copies and MMAs already in flight land before
+        // the shared memory and TMEM are released (bounded, ~1 ms)
+        const uint64_t t0 = ptx::globaltimer();
+        while (ptx::globaltimer() - t0 < 1000000ull) {
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int tile_partials_smem_bytes() { return kSmemBytes; }
+
+cudaError_t prepare_tile_partials_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_tile_partials<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
+}
+
+cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
+                                 const TilePartialsArgs& a, bool debug_logits, int num_sms,
+                                 cudaStream_t stream) {
+    const int num_m = (a.T + kTileM - 1) / kTileM;
+    const int num_n = (a.V_local + kTileN - 1) / kTileN;
+    const int64_t total = static_cast<int64_t>(num_m) * num_n;
+    const int grid = static_cast<int>(total < num_sms ? total : num_sms);
+    if (debug_logits)
+        k_tile_partials<true><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+    else
+        k_tile_partials<false><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+    return cudaGetLastError();
+}
+
+}  // namespace rlk

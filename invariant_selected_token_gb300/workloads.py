@@ -277,3 +277,22 @@ def bf16_tensor_bits(t) -> np.ndarray:
     """A torch bf16 tensor (any device) as a numpy uint16 bit array."""
     torch = _torch()
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def exact_device_case(T: int, H: int, V: int, device, seed: int, h_levels: int = 8,
+                      w_levels: int = 4) -> DeviceWorkload:
+    """Device-generated ``exact_case`` inputs at large sizes (hidden k/8, W j/64 grids)."""
+    torch = _torch()
+    assert H * h_levels * w_levels < (1 << 24)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    hid = (torch.randint(-h_levels, h_levels + 1, (T, H), generator=g, device=device)
+           .to(torch.float32) / 8.0).to(torch.bfloat16)
+    W = torch.empty((V, H), dtype=torch.bfloat16, device=device)
+    rows = 8192
+    for r0 in range(0, V, rows):
+        r1 = min(V, r0 + rows)
+        W[r0:r1] = (torch.randint(-w_levels, w_levels + 1, (r1 - r0, H), generator=g,
+                                  device=device).to(torch.float32) / 64.0).to(torch.bfloat16)
+    targets = torch.randint(0, V, (T,), generator=g, device=device).to(torch.int32)
+    return DeviceWorkload("exact_device", hid, W, targets, None, 1, {"seed": seed, "exact": True})

@@ -1,0 +1,134 @@
+"""Layout invariance on the GPU, compared bit for bit.
+
+A token's logprob and lse must not depend on the batch it is computed in
+(size, position, order), on the shard split of the vocabulary, on a decode
+(few rows) versus a packed launch, or on the run.  Every comparison is on
+the uint32 views: mismatch_count = 0 and max_abs_diff = 0.
+"""
+import numpy as np
+import pytest
+import torch
+
+from invariant_selected_token_gb300 import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(t):
+    return t.contiguous().view(torch.int32)
+
+
+def assert_same(a, b, what):
+    ia, ib = bits(a), bits(b)
+    mism = int((ia != ib).sum().item())
+    maxdiff = float((a.double() - b.double()).abs().max().item()) if a.numel() else 0.0
+    assert mism == 0 and maxdiff == 0.0, "%s: mismatch_count=%d max_abs_diff=%g" % (what, mism, maxdiff)
+
+
+def in_batches(rlk, hidden, W, targets, active, bsz, n_shards=1, order=None):
+    T = hidden.shape[0]
+    order = torch.arange(T, device=hidden.device) if order is None else order
+    lp = torch.empty(T, dtype=torch.float32, device=hidden.device)
+    lse = torch.empty_like(lp)
+    ws = rlk.new_workspace(min(bsz, T), W.shape[0], n_shards, hidden.device)
+    for b0 in range(0, T, bsz):
+        idx = order[b0:b0 + bsz]
+        act = None if active is None else active[idx].contiguous()
+        o_lp, o_lse = rlk.linear_logprob(hidden[idx].contiguous(), W, targets[idx].contiguous(), act,
+                                         n_shards, workspace=ws)
+        lp[idx] = o_lp
+        lse[idx] = o_lse
+    return lp, lse
+
+
+def sharded(rlk, hidden, W, targets, active, n):
+    V = W.shape[0]
+    parts = []
+    for r in range(n):
+        vb, ve = rlk.shard_range(V, n, r)
+        parts.append(rlk.linear_logprob_shard(hidden, W[vb:ve], targets, active, V, n, r))
+    return rlk.lse_merge(parts, active)
+
+
+@pytest.mark.parametrize("T,H,V", [(300, 256, 1000), (64, 256, 1024), (520, 512, 7777)])
+def test_small_invariance(rlk, cuda_device, T, H, V):
+    w = WL.to_device(WL.small_case(T, H, V, seed=T + V, inactive_frac=0.1), cuda_device)
+    ref_lp, ref_lse = rlk.linear_logprob(w.hidden, w.W, w.targets, w.active, 1)
+    for bsz in (1, 7, 64, 129):
+        for seed in (0, 1):
+            order = torch.from_numpy(WL.permutation(T, seed)).to(cuda_device)
+            lp, lse = in_batches(rlk, w.hidden, w.W, w.targets, w.active, bsz, 1, order)
+            assert_same(lp, ref_lp, "bsz=%d perm=%d" % (bsz, seed))
+            assert_same(lse, ref_lse, "bsz=%d perm=%d lse" % (bsz, seed))
+    nt = (V + 127) // 128
+    for n in (2, 4, 8):
+        if n > nt:
+            continue
+        lp, lse = rlk.linear_logprob(w.hidden, w.W, w.targets, w.active, n)
+        assert_same(lp, ref_lp, "n_shards=%d" % n)
+        lp, lse = sharded(rlk, w.hidden, w.W, w.targets, w.active, n)
+        assert_same(lp, ref_lp, "shard API n=%d" % n)
+        assert_same(lse, ref_lse, "shard API n=%d lse" % n)
+    for _ in range(3):
+        lp, lse = rlk.linear_logprob(w.hidden, w.W, w.targets, w.active, 1)
+        assert_same(lp, ref_lp, "repeat")
+
+
+def test_qwen_decode_rows_match_packed(rlk, qwen):
+    """Rollout-style decode batches (T = 1, 8, 64, 256) vs the same rows inside the packed batch."""
+    pk = qwen.packed
+    full_lp, full_lse = rlk.linear_logprob(pk.hidden, qwen.W, pk.targets, None, 4)
+    for T in (1, 8, 64, 256):
+        idx = torch.from_numpy(WL.decode_rows(T)).to(qwen.device)
+        lp, lse = rlk.linear_logprob(pk.hidden[idx].contiguous(), qwen.W,
+                                     pk.targets[idx].contiguous(), None, 1)
+        assert_same(lp, full_lp[idx], "decode T=%d" % T)
+        assert_same(lse, full_lse[idx], "decode T=%d lse" % T)
+
+
+def test_qwen_shard_api_matches_full(rlk, qwen):
+    pk = qwen.packed
+    full_lp, full_lse = rlk.linear_logprob(pk.hidden, qwen.W, pk.targets, None, 1)
+    for n in (2, 4, 8):
+        lp, lse = sharded(rlk, pk.hidden, qwen.W, pk.targets, None, n)
+        assert_same(lp, full_lp, "qwen shard API n=%d" % n)
+        assert_same(lse, full_lse, "qwen shard API n=%d lse" % n)
+        lp, lse = rlk.linear_logprob(pk.hidden, qwen.W, pk.targets, None, n)
+        assert_same(lp, full_lp, "qwen n_shards=%d" % n)
+
+
+@pytest.mark.slow
+def test_qwen_sweep_set(rlk, qwen):
+    """Fixed 8192-token set: batch sizes {1,7,64,1024,8192} x row orders x shard counts."""
+    sw = WL.sweep_set(qwen.W, qwen.device)
+    T = sw.hidden.shape[0]
+    ref_lp, ref_lse = rlk.linear_logprob(sw.hidden, qwen.W, sw.targets, None, 1)
+    # b = 1 over the first 512 tokens (each call is one row; order is immaterial)
+    lp, lse = in_batches(rlk, sw.hidden[:512], qwen.W, sw.targets[:512], None, 1)
+    assert_same(lp, ref_lp[:512], "b=1")
+    for bsz in (7, 64, 1024, 8192):
+        for seed in (11, 12, 13):
+            order = torch.from_numpy(WL.permutation(T, seed)).to(qwen.device)
+            lp, lse = in_batches(rlk, sw.hidden, qwen.W, sw.targets, None, bsz, 1, order)
+            assert_same(lp, ref_lp, "sweep b=%d perm=%d" % (bsz, seed))
+            assert_same(lse, ref_lse, "sweep b=%d perm=%d lse" % (bsz, seed))
+    for n in (2, 4, 8):
+        lp, lse = in_batches(rlk, sw.hidden, qwen.W, sw.targets, None, 1024, n,
+                             torch.from_numpy(WL.permutation(T, 20 + n)).to(qwen.device))
+        assert_same(lp, ref_lp, "sweep shards=%d" % n)
+
+
+def test_hidden_of_other_rows_cannot_leak(rlk, cuda_device):
+    """Inactive rows full of huge values leave every active row's bits unchanged."""
+    w = WL.to_device(WL.small_case(256, 256, 2000, seed=31), cuda_device)
+    ref_lp, ref_lse = rlk.linear_logprob(w.hidden, w.W, w.targets, None, 1)
+    hid = w.hidden.clone()
+    act = torch.ones(256, dtype=torch.uint8, device=cuda_device)
+    act[1::3] = 0
+    hid[1::3] = 3.0e38
+    tg = w.targets.clone()
+    tg[1::3] = -5  # never read for inactive rows
+    lp, lse = rlk.linear_logprob(hid, w.W, tg, act, 1)
+    keep = act.bool()
+    assert_same(lp[keep], ref_lp[keep], "active rows")
+    assert torch.all(lp[~keep] == 0) and torch.all(lse[~keep] == 0)
