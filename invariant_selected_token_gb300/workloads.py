@@ -80,6 +80,16 @@ def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
 
+# Independent device-generator streams per purpose: the weights, the hidden
+# rows and the target draws of one seed must not come from the same stream
+# (identical streams would make hidden row t a rescaled copy of W row t).
+_PURPOSE = {"weights": 1, "hidden": 2, "targets": 3}
+
+
+def _stream_seed(seed: int, purpose: str) -> int:
+    return (seed * 0x9E3779B1 + _PURPOSE[purpose] * 0x85EBCA77) % (1 << 62)
+
+
 # --------------------------------------------------------------------------
 # small numpy workloads (CPU tests and GPU parity at oracle-friendly sizes)
 # --------------------------------------------------------------------------
@@ -140,7 +150,7 @@ def head_weights(device, seed: int = 1234, V: int = V_QWEN3_8B, H: int = H_QWEN3
     """W ~ N(0, std) as bf16 [V, H] on ``device`` (seeded torch generator)."""
     torch = _torch()
     g = torch.Generator(device=device)
-    g.manual_seed(seed)
+    g.manual_seed(_stream_seed(seed, "weights"))
     W = torch.empty((V, H), dtype=torch.bfloat16, device=device)
     rows = 8192
     for r0 in range(0, V, rows):
@@ -154,7 +164,7 @@ def rms_hidden(T: int, H: int, device, seed: int):
     """Rows x / rms(x) with x ~ N(0,1), rounded to bf16."""
     torch = _torch()
     g = torch.Generator(device=device)
-    g.manual_seed(seed)
+    g.manual_seed(_stream_seed(seed, "hidden"))
     x = torch.randn((T, H), generator=g, device=device, dtype=torch.float32)
     x = x / torch.sqrt(torch.mean(x * x, dim=1, keepdim=True))
     return x.to(torch.bfloat16)
@@ -171,7 +181,7 @@ def topk_targets(hidden, W, seed: int, p_top: float = 0.9, k: int = 10):
     device = hidden.device
     T, V = hidden.shape[0], W.shape[0]
     g = torch.Generator(device=device)
-    g.manual_seed(seed + 7919)
+    g.manual_seed(_stream_seed(seed, "targets"))
     top_idx = torch.empty((T, k), dtype=torch.int64, device=device)
     rows = 2048
     for r0 in range(0, T, rows):
