@@ -207,6 +207,35 @@ rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, 
 rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
                               float* out_logits, int32_t* dev_status, rlk_stream_t stream);
 
+/*
+ * Same result as rlk_linear_logprob (same kernels, same bits), for callers
+ * that cannot allocate device memory when they call: e.g. a rollout engine
+ * that reserved almost all GPU memory for its KV cache at start-up, or a
+ * decode loop that cannot afford the device-wide synchronisation cudaFree
+ * performs.  Instead of a caller workspace it uses a scratch array of
+ * RLK_STATIC_WS_BYTES compiled into the library (one copy per GPU that
+ * loads the library, held until the process exits).  The pages have no
+ * counterpart to this call; it is a deployment convenience.
+ *
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Batches whose workspace (rlk_workspace_size(T, V, n_shards)) exceeds
+ *     RLK_STATIC_WS_BYTES are refused with RLK_ERR_WORKSPACE; at V = 151936
+ *     that is about 1700 tokens per call with 4 shards.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     (e.g. on two unordered streams) race; order them.  Nothing in the
+ *     array needs to start at zero.
+ * Other arguments and errors as rlk_linear_logprob.
+ */
+#define RLK_STATIC_WS_BYTES (16u << 20)
+rlk_status_t rlk_linear_logprob_static_ws(const void* hidden, const void* W,
+                                          const int32_t* targets, const uint8_t* active_mask,
+                                          int64_t T, int64_t H, int64_t V, int n_shards,
+                                          float* out_logprob, float* out_lse, int32_t* dev_status,
+                                          rlk_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,8 @@ VOCAB_TILE = 128
 
 EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rlk_shard_range",
             "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
-            "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits"]
+            "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
+            "rlk_linear_logprob_static_ws"]
 
 
 class RlkError(RuntimeError):
