@@ -40,9 +40,13 @@ WORKLOAD = "packed training batch T=4096 (8x512), H=4096, V=151936, bf16, 4 voca
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
+    p.add_argument("--workload", default="packed",
+                   choices=["packed", "decode1", "decode8", "decode64", "decode256"],
+                   help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
+                        "as a rollout-side decode batch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -64,7 +68,7 @@ def load_peaks():
 class ClockSampler:
     """nvidia-smi clock / throttle samples during the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -88,7 +92,8 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between host times t0 and t1 (all if too few)."""
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -97,30 +102,37 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows = []
         for line in self.lines:
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), float(f[4]) if f[4] else 0.0, f[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        use = inside if len(inside) >= 2 else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for n, v in zip(names, r[4]):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "power_w_max": max(r[3] for r in use), "samples": len(use),
+                "samples_in_timed_region": len(inside), "reasons": sorted(reasons)}
 
 
-def k1_traffic_record():
-    """Per-launch DRAM bytes of the tile-partials kernel from the committed ncu summary,
-    if it was taken from the library build that is loaded now (else None)."""
-    path = os.path.join(ROOT, "profiles", "tile_partials_packed_T4096.md")
+def k1_traffic_record(workload):
+    """Per-launch DRAM bytes of the tile-partials kernel from the committed ncu summary of
+    this workload, if it was taken from the library build that is loaded now (else None)."""
+    path = os.path.join(ROOT, "profiles", "tile_partials_%s.md" % workload)
     try:
         from invariant_selected_token_gb300 import binding
         digest = binding.build_fingerprint().split("rev=")[1].split(";")[0]
@@ -130,8 +142,9 @@ def k1_traffic_record():
                 if ":" in line and line.strip().startswith("- "):
                     k, v = line.strip()[2:].split(":", 1)
                     rec[k.strip()] = v.strip().strip("`")
-        if rec.get("library_rev") == digest:
-            return int(rec["dram_bytes_per_launch"])
+        if rec.get("library_rev", "").split()[0].strip("`") == digest:
+            import re
+            return int(re.search(r"\d+", rec["dram_bytes_per_launch"]).group(0))
     except Exception:
         pass
     return None
@@ -219,7 +232,16 @@ def main():
 
     W = WL.head_weights(dev)                       # same weights on every rank
     pk = WL.packed(W, dev, seed=1234 + 1000 * rank)  # each rank its own batch
-    T = pk.hidden.shape[0]
+    if args.workload == "packed":
+        hidden, targets = pk.hidden, pk.targets
+        workload = WORKLOAD
+    else:
+        n = int(args.workload[len("decode"):])
+        idx = torch.from_numpy(WL.decode_rows(n)).to(dev)
+        hidden, targets = pk.hidden[idx].contiguous(), pk.targets[idx].contiguous()
+        workload = ("decode batch T=%d (rows of the packed batch), H=4096, V=151936, bf16, "
+                    "4 vocab shards" % n)
+    T = hidden.shape[0]
     ws = binding.new_workspace(T, V, N_SHARDS, dev)
     out_lp = torch.empty(T, dtype=torch.float32, device=dev)
     out_lse = torch.empty(T, dtype=torch.float32, device=dev)
@@ -229,10 +251,10 @@ def main():
     def step(ev0=None, ev1=None):
         if ev0 is not None:
             ev0.record(stream)
-        binding.tile_partials(pk.hidden, W, pk.targets, None, N_SHARDS, ws, status, stream)
+        binding.tile_partials(hidden, W, targets, None, N_SHARDS, ws, status, stream)
         if ev1 is not None:
             ev1.record(stream)
-        binding.tile_merge(pk.targets, None, V, N_SHARDS, out_lp, out_lse, ws, status, stream)
+        binding.tile_merge(targets, None, V, N_SHARDS, out_lp, out_lse, ws, status, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -250,12 +272,14 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    t_host0 = time.time()
     start.record(stream)
     for k in range(K):
         step(*k1_ev[k])
     end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    t_host1 = time.time()
+    clk = clocks.stop(t_host0, t_host1)
     if dist is not None:
         dist.barrier()
     ms_total = start.elapsed_time(end)
@@ -271,12 +295,12 @@ def main():
     # ---------------- end to end through the public call, host buffers
     e2e = None
     if not args.no_e2e:
-        h_hidden = pk.hidden.cpu().pin_memory()
-        h_tg = pk.targets.cpu().pin_memory()
+        h_hidden = hidden.cpu().pin_memory()
+        h_tg = targets.cpu().pin_memory()
         h_lp = torch.empty(T, dtype=torch.float32).pin_memory()
         h_lse = torch.empty(T, dtype=torch.float32).pin_memory()
-        d_hidden = torch.empty_like(pk.hidden)
-        d_tg = torch.empty_like(pk.targets)
+        d_hidden = torch.empty_like(hidden)
+        d_tg = torch.empty_like(targets)
 
         def e2e_step():
             d_hidden.copy_(h_hidden, non_blocking=True)
@@ -307,33 +331,41 @@ def main():
     # ---------------- roofline of the dominant kernel (logits GEMM + fused epilogue)
     peaks = load_peaks()
     flops = 2.0 * T * H * V
-    achieved_tflops = flops / (k1_ms / 1000.0) / 1e12
-    peak = peaks["bf16_tflops"]
-    traffic = k1_traffic_record()
-    roofline = {"bound": "tensor", "achieved": round(achieved_tflops, 1), "peak": peak,
-                "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4), "traffic": traffic,
-                "kernel": "k_tile_partials", "kernel_ms": round(k1_ms, 4),
-                "peak_kind": "burst bf16 (%s)" % peaks["source"],
-                "frac_of_sustained": round(achieved_tflops / peaks["bf16_tflops_sustained"], 4)}
-    step_roof_ms = max(flops / (peak * 1e12), (W.numel() * 2 + pk.hidden.numel() * 2)
-                       / (peaks["hbm_gbs"] * 1e9)) * 1000.0
+    nbytes = float(W.numel() * 2 + hidden.numel() * 2)
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    traffic = k1_traffic_record(args.workload)
+    if t_tensor >= t_hbm:
+        achieved = flops / (k1_ms / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "traffic": traffic, "peak_kind": "burst bf16 (%s)" % peaks["source"],
+                    "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+    else:
+        achieved = nbytes / (k1_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": traffic, "peak_kind": "copy bandwidth (%s)" % peaks["source"]}
+    roofline.update({"kernel": "k_tile_partials", "kernel_ms": round(k1_ms, 4),
+                     "algorithmic": {"flops": flops, "bytes": nbytes}})
+    step_roof_ms = max(t_tensor, t_hbm) * 1000.0
 
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W_bits = WL.bf16_tensor_bits(W)
-        rows = WL.permutation(T, 4321)[:24]
-        hid_bits = WL.bf16_tensor_bits(pk.hidden[torch.from_numpy(rows).to(dev)])
-        s, n = cpu_oracle_sample(hid_bits, W_bits, pk.targets.cpu().numpy()[rows], None)
-        cpu = {"value": n / s, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": "%d rows of the packed batch over the full vocabulary (%.1f s)" % (n, s)}
+        rows = WL.permutation(T, 4321)[:min(T, 24)]
+        hid_bits = WL.bf16_tensor_bits(hidden[torch.from_numpy(rows).to(dev)])
+        s_, n_ = cpu_oracle_sample(hid_bits, W_bits, targets.cpu().numpy()[rows], None)
+        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "%d rows of the batch over the full vocabulary (%.1f s)" % (n_, s_)}
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
                "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                "dtype": "bf16", "data": "synthetic",
-               "config": {"workload": WORKLOAD, "T": T, "H": H, "V": V, "n_shards": N_SHARDS,
+               "config": {"workload": workload, "T": T, "H": H, "V": V, "n_shards": N_SHARDS,
                           "accumulate": "fp32", "l2": "inputs larger than L2 (W = 1.24 GB)",
                           "parallelism": "dp%d (independent batches)" % world,
                           "roofline_step_ms": round(step_roof_ms, 4),
