@@ -156,7 +156,10 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
                                int64_t v_offset, float2* partials, float* tgt, float* dbg,
                                int32_t* status, cudaStream_t stream, const DeviceState* dev) {
     CUtensorMap map_h, map_w;
-    rlk_status_t s = encode_bf16_map(&map_h, hidden, H, T, kTileM);
+    // one token tile: load only the rows that exist (rounded up to a whole
+    // 8-row swizzle atom); the MMA's other accumulator rows are discarded
+    const int a_rows = T >= kTileM ? kTileM : int((T + 7) / 8 * 8);
+    rlk_status_t s = encode_bf16_map(&map_h, hidden, H, T, uint32_t(a_rows));
     if (s != RLK_OK) return s;
     s = encode_bf16_map(&map_w, W, H, V_local, kTileN);
     if (s != RLK_OK) return s;
@@ -172,6 +175,7 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     a.V_local = int(V_local);
     a.n_tiles = int(n_tiles_of(V_local));
     a.k_blocks = int(H / rlk::kBlockK);
+    a.a_box_rows = a_rows;
     return rlk::launch_tile_partials(map_h, map_w, a, dbg != nullptr, dev->sm_count, stream) ==
                    cudaSuccess
                ? RLK_OK

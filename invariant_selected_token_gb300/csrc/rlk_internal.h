@@ -29,6 +29,7 @@ struct TilePartialsArgs {
     int V_local;              // rows of W this launch covers
     int n_tiles;              // ceil(V_local / 128): row stride of partials
     int k_blocks;             // H / 64
+    int a_box_rows;           // rows of the hidden TMA box: 128, or roundup(T, 8) when T <= 128
 };
 
 // hidden map: bf16 [T][H], box 64 x 128; weight map: bf16 [V_local][H], box 64 x 256.

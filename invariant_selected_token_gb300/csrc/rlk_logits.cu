@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
+            // A batch of at most 128 tokens loads only its first roundup(T, 8)
+            // hidden rows; the accumulator rows beyond them are never read.
+            const uint32_t a_bytes = static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2;
             uint32_t stage = 0, phase = 0;
             for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
                 const int n_blk = tile / num_m;
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         report(a.status, RLK_ERR_TIMEOUT);
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(&full[stage], kStageBytesA + kStageBytesB);
+                    ptx::mbar_arrive_expect_tx(&full[stage], a_bytes + kStageBytesB);
                     ptx::tma_load_2d(sA + stage * kStageBytesA, &map_hidden, &full[stage],
                                      kb * kBlockK, m_blk * kTileM);
                     ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],

@@ -132,3 +132,28 @@ def test_hidden_of_other_rows_cannot_leak(rlk, cuda_device):
     keep = act.bool()
     assert_same(lp[keep], ref_lp[keep], "active rows")
     assert torch.all(lp[~keep] == 0) and torch.all(lse[~keep] == 0)
+
+
+@pytest.mark.parametrize("T,H,V", [(5, 128, 1000), (300, 256, 40000), (64, 512, 262144),
+                                   (9, 64, 129)])
+def test_tree_layouts_agree(rlk, cuda_device, monkeypatch, T, H, V):
+    """One warp per token and one CTA per token evaluate the same tree: same bits, records too."""
+    w = WL.to_device(WL.small_case(T, H, V, seed=T + 3, w_std=0.05, inactive_frac=0.2), cuda_device)
+    nt = (V + 127) // 128
+    for n in (1, 2, 4, 8):
+        if n > nt:
+            continue
+        outs = []
+        for threads in ("32", "256"):
+            monkeypatch.setenv("RLK_TEST_TREE_THREADS", threads)
+            ws = rlk.new_workspace(T, V, n, cuda_device)
+            lp, lse = rlk.linear_logprob(w.hidden, w.W, w.targets, w.active, n, workspace=ws)
+            vb, ve = rlk.shard_range(V, n, n - 1)
+            part = rlk.linear_logprob_shard(w.hidden, w.W[vb:ve], w.targets, w.active, V, n, n - 1)
+            outs.append((lp, lse, rlk.workspace_records(ws, T, V, n).clone(), part))
+        monkeypatch.delenv("RLK_TEST_TREE_THREADS")
+        (a_lp, a_lse, a_rec, a_part), (b_lp, b_lse, b_rec, b_part) = outs
+        assert_same(a_lp, b_lp, "logprob n=%d" % n)
+        assert_same(a_lse, b_lse, "lse n=%d" % n)
+        assert torch.equal(a_rec, b_rec), "records n=%d" % n
+        assert torch.equal(a_part, b_part), "shard record n=%d" % n
