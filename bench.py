@@ -150,6 +150,26 @@ def k1_traffic_record(workload):
     return None
 
 
+def rank_batch_seed(rank: int) -> int:
+    """Seed of a rank's own batch: ranks share W but never a token."""
+    return 1234 + 1000 * rank
+
+
+def max_over_ranks(ms: float, dist, device) -> float:
+    """The slowest rank's time (every rank gets it); identity without a process group."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, ms_total: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms_total / 1000.0)
+
+
 def cpu_oracle_sample(hidden_bits, W_bits, targets, rows):
     """Time the fp64 oracle on the listed rows; returns (seconds, rows)."""
     from oracle import linear_logprob as oracle
@@ -231,7 +251,7 @@ def main():
     binding.lib()
 
     W = WL.head_weights(dev)                       # same weights on every rank
-    pk = WL.packed(W, dev, seed=1234 + 1000 * rank)  # each rank its own batch
+    pk = WL.packed(W, dev, seed=rank_batch_seed(rank))  # each rank its own batch
     if args.workload == "packed":
         hidden, targets = pk.hidden, pk.targets
         workload = WORKLOAD
@@ -285,12 +305,9 @@ def main():
     ms_total = start.elapsed_time(end)
     k1_ms = statistics.mean(a.elapsed_time(b) for a, b in k1_ev)
     binding.raise_on_device_status(status)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_per_step = ms_total / K
-    value = world * T * K / (ms_total / 1000.0)
+    value = weak_scaling_value(world, T, K, ms_total)
 
     # ---------------- end to end through the public call, host buffers
     e2e = None
@@ -320,11 +337,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * T * K / (e_ms / 1000.0), "unit": "tokens/s",
+        e_ms = max_over_ranks(e_ms, dist, dev)
+        e2e = {"value": weak_scaling_value(world, T, K, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h_hidden.numel() * 2 + h_tg.numel() * 4),
                "d2h_bytes_per_step": int(T * 4 * 2)}
 
