@@ -44,9 +44,11 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
-                   choices=["packed", "decode1", "decode8", "decode64", "decode256"],
+                   choices=["packed", "decode1", "decode8", "decode64", "decode256",
+                            "logits_fp32", "logits_bf16"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
-                        "as a rollout-side decode batch")
+                        "as a rollout-side decode batch; logits_*: the same batch's logits "
+                        "materialised in HBM, reduced by the materialised-logits path")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -223,6 +225,83 @@ def reference_arm(args, rank, world):
     return 0
 
 
+# FP32 lanes per SM (4 sub-partitions x 32) -- the ALU roofline's unit count.
+FP32_LANES_PER_SM = 128
+# Contract operations per logit on the materialised path: exp (2 fma + 1 sub
+# for the reduction, 2 fma for r, 7 fma Horner, 1 mul scale, 1 integer
+# exponent build, 1 compare/select) + subtract-max + max + tree add.
+OPS_PER_LOGIT = 19
+
+
+def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
+    """Selected logprob from the packed batch's logits materialised in HBM."""
+    import torch
+    T = pk.hidden.shape[0]
+    L = binding.debug_logits(pk.hidden, W)
+    if args.workload == "logits_bf16":
+        L = L.to(torch.bfloat16)
+    del W
+    torch.cuda.empty_cache()
+    ws = binding.new_workspace(T, V, N_SHARDS, dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.logits_logprob(L, pk.targets, None, N_SHARDS, lp, lse, ws, status, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(t0, time.time())
+    ms_total = sum(a.elapsed_time(b) for a, b in ev)
+    ms_total = max_over_ranks(ms_total, dist, dev)
+    call_ms = ms_total / K
+    nbytes = float(L.numel() * L.element_size())
+    peak_ops = FP32_LANES_PER_SM * torch.cuda.get_device_properties(dev).multi_processor_count \
+        * 2.07e9
+    achieved_ops = OPS_PER_LOGIT * T * V / (call_ms / 1000.0)
+    peaks = load_peaks()
+    if rank == 0:
+        out = {"metric": METRIC, "value": weak_scaling_value(world, T, K, ms_total),
+               "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+               "ms_per_step": call_ms, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "f32" if args.workload == "logits_fp32" else "bf16",
+               "data": "synthetic",
+               "config": {"workload": "materialised logits of the packed batch (T=4096, "
+                                      "V=151936, %s), 4 vocab shards" % args.workload[7:],
+                          "T": T, "V": V, "n_shards": N_SHARDS,
+                          "l2": "inputs larger than L2 (logits %.2f GB)" % (nbytes / 1e9)},
+               "roofline": {"bound": "alu", "achieved": round(achieved_ops / 1e9, 1),
+                            "peak": round(peak_ops / 1e9, 1), "unit": "Gop/s",
+                            "frac": round(achieved_ops / peak_ops, 4), "traffic": None,
+                            "kernel": "k_mat_tile_partials + k_tile_tree (whole call)",
+                            "ops_per_logit": OPS_PER_LOGIT,
+                            "hbm_GBps": round(nbytes / (call_ms / 1000.0) / 1e9, 1),
+                            "hbm_frac": round(nbytes / (call_ms / 1000.0) / 1e9 / peaks["hbm_gbs"], 4)},
+               "cpu_baseline": None, "e2e": None, "gpu_launches": 2 * K, "clocks": clk,
+               "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out))
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -261,6 +340,8 @@ def main():
         hidden, targets = pk.hidden[idx].contiguous(), pk.targets[idx].contiguous()
         workload = ("decode batch T=%d (rows of the packed batch), H=4096, V=151936, bf16, "
                     "4 vocab shards" % n)
+    if args.workload.startswith("logits_"):
+        return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
     T = hidden.shape[0]
     ws = binding.new_workspace(T, V, N_SHARDS, dev)
     out_lp = torch.empty(T, dtype=torch.float32, device=dev)

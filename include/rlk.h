@@ -92,6 +92,8 @@ typedef struct rlk_partial {
 #define RLK_MAX_SHARDS 8
 #define RLK_MAX_VOCAB 262144          /* 2048 tiles */
 #define RLK_K_BLOCK 64                /* H must be a multiple of this */
+#define RLK_DTYPE_F32 0               /* logits element types for the materialised-logits calls */
+#define RLK_DTYPE_BF16 1
 
 /* "rlk-linlogp-v1": names the numeric contract above. */
 const char* rlk_contract_id(void);
@@ -206,6 +208,42 @@ rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, 
  */
 rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
                               float* out_logits, int32_t* dev_status, rlk_stream_t stream);
+
+/*
+ * Selected-token logprob from logits that already exist in memory, under
+ * the same contract (the blog's rl_kernel.log_softmax with a fixed reduction
+ * tree, sections 4.2-4.3, read at the target).  Given the fp32 logits the
+ * fused path computes (rlk_debug_logits), it returns the fused path's bits.
+ *
+ *   logits       device, [T][ld] row-major, elements RLK_DTYPE_F32 or RLK_DTYPE_BF16
+ *                (bf16 widens exactly to fp32); only columns [0, V) are read
+ *   ld           row stride in elements, >= V; logits aligned to their element
+ *                size (rows that start on 16-byte (fp32) / 8-byte (bf16)
+ *                boundaries, i.e. ld % 4 == 0 on an aligned base, are read with
+ *                vector loads; the values and results are the same either way)
+ *   workspace    >= rlk_workspace_size(T, V, n_shards) bytes, same layout as rlk_linear_logprob
+ * Other arguments, outputs and errors as rlk_linear_logprob.
+ */
+rlk_status_t rlk_logits_logprob(const void* logits, int logits_dtype, int64_t ld,
+                                const int32_t* targets, const uint8_t* active_mask, int64_t T,
+                                int64_t V, int n_shards, float* out_logprob, float* out_lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                rlk_stream_t stream);
+
+/*
+ * Full log_softmax of materialised logits: out[t][v] = RN(l[t][v] - lse[t])
+ * with lse from the contract's tile tree; out_lse[t] = lse[t].  Inactive rows
+ * give zeros.  The same tree gives the same lse bits as rlk_linear_logprob.
+ *
+ *   out          device, float [T][V] row-major (dense, V columns)
+ *   out_lse      device, float [T]
+ *   workspace    >= rlk_workspace_size(T, V, 1) bytes
+ * logits, logits_dtype, ld as rlk_logits_logprob.
+ */
+rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
+                             const uint8_t* active_mask, int64_t T, int64_t V, float* out,
+                             float* out_lse, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, rlk_stream_t stream);
 
 /*
  * Same result as rlk_linear_logprob (same kernels, same bits), for callers

@@ -28,7 +28,8 @@ VOCAB_TILE = 128
 EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rlk_shard_range",
             "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
             "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
-            "rlk_linear_logprob_static_ws"]
+            "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax"]
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 
 class RlkError(RuntimeError):
@@ -71,6 +72,10 @@ def lib() -> ctypes.CDLL:
         L.rlk_tile_merge.argtypes = [P, P, i64, i64, i32, P, P, P, sz, P, P]
         L.rlk_debug_logits.restype = i32
         L.rlk_debug_logits.argtypes = [P, P, i64, i64, i64, P, P, P]
+        L.rlk_logits_logprob.restype = i32
+        L.rlk_logits_logprob.argtypes = [P, i32, i64, P, P, i64, i64, i32, P, P, P, sz, P, P]
+        L.rlk_log_softmax.restype = i32
+        L.rlk_log_softmax.argtypes = [P, i32, i64, P, i64, i64, P, P, P, sz, P, P]
         _lib = L
     return _lib
 
@@ -256,3 +261,50 @@ def debug_logits(hidden: torch.Tensor, W: torch.Tensor, status=None, stream=None
 
 def shard_ranges(V: int, n_shards: int) -> List[Tuple[int, int]]:
     return [shard_range(V, n_shards, r) for r in range(n_shards)]
+
+
+def _logits_view(logits: torch.Tensor, V: Optional[int]):
+    if logits.dtype not in DTYPES:
+        raise TypeError("logits must be float32 or bfloat16")
+    if not logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D CUDA tensor with unit column stride")
+    T = logits.shape[0]
+    V = logits.shape[1] if V is None else V
+    return T, V, logits.stride(0) if T > 1 else V
+
+
+def logits_logprob(logits: torch.Tensor, targets: torch.Tensor, active=None, n_shards: int = 1,
+                   out_logprob=None, out_lse=None, workspace=None, status=None, stream=None
+                   ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(logprob, lse) of materialised fp32/bf16 logits [T, V] (rows may be padded)."""
+    dev = logits.device
+    T, V, ld = _logits_view(logits, None)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, V, n_shards, dev)
+    _check(lib().rlk_logits_logprob(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(targets),
+                                    _ptr(active), T, V, n_shards, _ptr(out_logprob), _ptr(out_lse),
+                                    _ptr(workspace), workspace.numel(), _ptr(status),
+                                    _stream(dev, stream)), "rlk_logits_logprob")
+    return out_logprob, out_lse
+
+
+def log_softmax(logits: torch.Tensor, active=None, out=None, out_lse=None, workspace=None,
+                status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(log_softmax [T, V] fp32, lse [T]) of materialised fp32/bf16 logits."""
+    dev = logits.device
+    T, V, ld = _logits_view(logits, None)
+    if out is None:
+        out = torch.empty((T, V), dtype=torch.float32, device=dev)
+    if out_lse is None:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, V, 1, dev)
+    _check(lib().rlk_log_softmax(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(active), T, V,
+                                 _ptr(out), _ptr(out_lse), _ptr(workspace), workspace.numel(),
+                                 _ptr(status), _stream(dev, stream)), "rlk_log_softmax")
+    return out, out_lse

@@ -191,6 +191,53 @@ rlk_status_t common_checks(const void* hidden, const void* W, const int32_t* tar
     return RLK_OK;
 }
 
+// Tile tree over a full-vocabulary workspace (layout_of(T, V, n_shards)):
+// shard records, then lse (and logprob when targets is not null).
+rlk_status_t run_tile_tree(const int32_t* targets, const uint8_t* active, int64_t T, int64_t V,
+                           int n_shards, float* out_logprob, float* out_lse, uint8_t* ws,
+                           const Layout& l, int32_t* status, cudaStream_t stream) {
+    const int64_t nt = n_tiles_of(V);
+    rlk::TileTreeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.partials = reinterpret_cast<const float2*>(ws + l.partials);
+    a.ld = nt;
+    a.tgt_logit = reinterpret_cast<const float*>(ws + l.tgt);
+    a.targets = targets;
+    a.active = active;
+    a.status = status;
+    a.T = int(T);
+    a.n_tiles = int(nt);
+    a.depth = tree_depth(nt);
+    a.shard_depth = log2_exact(n_shards);
+    a.n_shards = n_shards;
+    a.shard_mode = 0;
+    for (int r = 0; r < n_shards; ++r) {
+        int64_t b = 0, e = 0;
+        int64_t first = 0, count = 0;
+        tree_node(nt, log2_exact(n_shards), r, &first, &count);
+        b = first * kVocabTile;
+        e = (first + count) * kVocabTile < V ? (first + count) * kVocabTile : V;
+        a.shard_vbegin[r] = b;
+        a.shard_vbegin[r + 1] = e;
+    }
+    a.V_total = V;
+    a.out_logprob = out_logprob;
+    a.out_lse = out_lse;
+    a.records = reinterpret_cast<rlk_partial_t*>(ws + l.records);
+    return rlk::launch_tile_tree(a, stream) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+// Checks shared by the two materialised-logits calls.
+rlk_status_t mat_checks(const void* logits, int dtype, int64_t ld, int64_t T, int64_t V) {
+    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    if (V < 1 || ld < V) return RLK_ERR_INVALID_ARG;
+    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
+    if (dtype != RLK_DTYPE_F32 && dtype != RLK_DTYPE_BF16) return RLK_ERR_UNSUPPORTED;
+    if (T > 0 && !logits) return RLK_ERR_INVALID_ARG;
+    if (!aligned(logits, dtype == RLK_DTYPE_F32 ? 4 : 2)) return RLK_ERR_ALIGNMENT;
+    return RLK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -273,35 +320,9 @@ rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, 
     if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
     DeviceState* dev = nullptr;
     if ((s = device_check(&dev)) != RLK_OK) return s;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const int64_t nt = n_tiles_of(V);
-    rlk::TileTreeArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.partials = reinterpret_cast<const float2*>(ws + l.partials);
-    a.ld = nt;
-    a.tgt_logit = reinterpret_cast<const float*>(ws + l.tgt);
-    a.targets = targets;
-    a.active = active_mask;
-    a.status = dev_status;
-    a.T = int(T);
-    a.n_tiles = int(nt);
-    a.depth = tree_depth(nt);
-    a.shard_depth = log2_exact(n_shards);
-    a.n_shards = n_shards;
-    a.shard_mode = 0;
-    for (int r = 0; r < n_shards; ++r) {
-        int64_t b = 0, e = 0;
-        rlk_shard_range(V, n_shards, r, &b, &e);
-        a.shard_vbegin[r] = b;
-        a.shard_vbegin[r + 1] = e;
-    }
-    a.V_total = V;
-    a.out_logprob = out_logprob;
-    a.out_lse = out_lse;
-    a.records = reinterpret_cast<rlk_partial_t*>(ws + l.records);
-    return rlk::launch_tile_tree(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? RLK_OK
-               : RLK_ERR_CUDA;
+    return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse,
+                         static_cast<uint8_t*>(workspace), l, dev_status,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 rlk_status_t rlk_linear_logprob(const void* hidden, const void* W, const int32_t* targets,
@@ -406,6 +427,62 @@ rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int6
     if ((s = device_check(&dev)) != RLK_OK) return s;
     return run_tile_partials(hidden, W, nullptr, nullptr, T, H, V, 0, nullptr, nullptr, out_logits,
                              dev_status, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+rlk_status_t rlk_logits_logprob(const void* logits, int logits_dtype, int64_t ld,
+                                const int32_t* targets, const uint8_t* active_mask, int64_t T,
+                                int64_t V, int n_shards, float* out_logprob, float* out_lse,
+                                void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                rlk_stream_t stream) {
+    rlk_status_t s = mat_checks(logits, logits_dtype, ld, T, V);
+    if (s != RLK_OK) return s;
+    if ((s = shard_check(V, n_shards)) != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!targets || !out_logprob || !out_lse || !workspace) return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(targets, 4)) return RLK_ERR_ALIGNMENT;
+    const Layout l = layout_of(T, V, n_shards);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (rlk::launch_mat_tile_partials(logits, logits_dtype, ld, targets, active_mask, int(T),
+                                      int(V), reinterpret_cast<float2*>(ws + l.partials),
+                                      reinterpret_cast<float*>(ws + l.tgt), dev->sm_count,
+                                      st) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse, ws, l,
+                         dev_status, st);
+}
+
+rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
+                             const uint8_t* active_mask, int64_t T, int64_t V, float* out,
+                             float* out_lse, void* workspace, size_t workspace_bytes,
+                             int32_t* dev_status, rlk_stream_t stream) {
+    rlk_status_t s = mat_checks(logits, logits_dtype, ld, T, V);
+    if (s != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!out || !out_lse || !workspace) return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(out, 4) || !aligned(out_lse, 4))
+        return RLK_ERR_ALIGNMENT;
+    const Layout l = layout_of(T, V, 1);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (rlk::launch_mat_tile_partials(logits, logits_dtype, ld, nullptr, active_mask, int(T),
+                                      int(V), reinterpret_cast<float2*>(ws + l.partials),
+                                      reinterpret_cast<float*>(ws + l.tgt), dev->sm_count,
+                                      st) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    if ((s = run_tile_tree(nullptr, active_mask, T, V, 1, nullptr, out_lse, ws, l, dev_status,
+                           st)) != RLK_OK)
+        return s;
+    return rlk::launch_log_softmax_out(logits, logits_dtype, ld, out_lse, active_mask, int(T),
+                                       int(V), out, dev->sm_count, st) == cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
 }
 
 }  // extern "C"

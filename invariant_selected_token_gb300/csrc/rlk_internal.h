@@ -43,7 +43,7 @@ struct TileTreeArgs {
     const float2* partials;   // [T][ld]
     int64_t ld;
     const float* tgt_logit;   // [T]
-    const int32_t* targets;   // [T]
+    const int32_t* targets;   // [T], or nullptr: lse only (no target, no logprob)
     const uint8_t* active;    // [T] or nullptr
     int32_t* status;
     int T;
@@ -61,6 +61,16 @@ struct TileTreeArgs {
 };
 
 cudaError_t launch_tile_tree(const TileTreeArgs& a, cudaStream_t stream);
+
+// materialised logits [T][ld] (fp32 or bf16) -> the same per-tile pairs / target logits
+cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
+                                     const int32_t* targets, const uint8_t* active, int T, int V,
+                                     float2* partials, float* tgt_logit, int num_sms,
+                                     cudaStream_t stream);
+// out[t][v] = RN(l[t][v] - lse[t])
+cudaError_t launch_log_softmax_out(const void* logits, int dtype, int64_t ld, const float* lse,
+                                   const uint8_t* active, int T, int V, float* out, int num_sms,
+                                   cudaStream_t stream);
 
 struct ShardMergeArgs {
     const rlk_partial_t* parts[RLK_MAX_SHARDS];

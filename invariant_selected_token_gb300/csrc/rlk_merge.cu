@@ -124,20 +124,24 @@ __device__ __forceinline__ void write_inactive(const TileTreeArgs& a, int t) {
     } else {
         for (int r = 0; r < a.n_shards; ++r)
             a.records[static_cast<int64_t>(r) * a.T + t] = rlk_partial_t{0.0f, 0.0f, 0.0f, 0u};
-        a.out_logprob[t] = 0.0f;
+        if (a.out_logprob) a.out_logprob[t] = 0.0f;
         a.out_lse[t] = 0.0f;
     }
 }
 
 __device__ __forceinline__ void write_shard_record(const TileTreeArgs& a, int t, int r, MaxSum n) {
-    const int64_t tg = a.targets[t];
-    const bool owned = tg >= a.shard_vbegin[r] && tg < a.shard_vbegin[r + 1];
+    const int64_t tg = a.targets ? a.targets[t] : -1;
+    const bool owned = a.targets && tg >= a.shard_vbegin[r] && tg < a.shard_vbegin[r + 1];
     a.records[static_cast<int64_t>(r) * a.T + t] =
         rlk_partial_t{n.m, n.s, owned ? a.tgt_logit[t] : 0.0f, owned ? 1u : 0u};
 }
 
 // Root of a token's tree -> its shard-mode record, or the final lse / logprob.
 __device__ __forceinline__ void finish_token(const TileTreeArgs& a, int t, MaxSum root) {
+    if (!a.targets) {  // log_softmax: the log-sum-exp alone
+        a.out_lse[t] = __fadd_rn(root.m, contract_log(root.s));
+        return;
+    }
     const int64_t tg = a.targets[t];
     if (a.shard_mode) {
         const bool owned = tg >= a.own_begin && tg < a.own_end;

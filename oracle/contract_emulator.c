@@ -270,6 +270,22 @@ int emu_linear_logprob(const float* logits, int64_t T, int64_t V, const int32_t*
     return 0;
 }
 
+/* log_softmax: out[t][v] = RN(l - lse) with lse from the full tile tree; inactive rows 0 */
+int emu_log_softmax(const float* logits, int64_t T, int64_t V, const uint8_t* active,
+                    float* out, float* out_lse) {
+    int32_t* tg = (int32_t*)calloc((size_t)(T > 0 ? T : 1), sizeof(int32_t));
+    int rc = emu_linear_logprob(logits, T, V, tg, active, 1, NULL, out_lse, NULL, NULL, NULL, NULL,
+                                NULL, NULL);
+    free(tg);
+    if (rc != 0) return rc;
+    for (int64_t t = 0; t < T; ++t) {
+        int act = active ? (active[t] != 0) : 1;
+        for (int64_t v = 0; v < V; ++v)
+            out[t * V + v] = act ? logits[t * V + v] - out_lse[t] : 0.0f;
+    }
+    return 0;
+}
+
 /* ---- exhaustive accuracy sweeps against fp64 libm (the independent reference) ---- */
 static double ulp_err(float y, double z) {
     if (z == 0.0) return y == 0.0f ? 0.0 : INFINITY;

@@ -44,6 +44,8 @@ def lib():
             fn = getattr(L, name)
             fn.restype = None
             fn.argtypes = [f, f, P, P, P]
+        L.emu_log_softmax.restype = i32
+        L.emu_log_softmax.argtypes = [P, i64, i64, P, P, P]
         L.emu_constants.restype = None
         L.emu_constants.argtypes = [P]
         _lib = L
@@ -130,6 +132,19 @@ def linear_logprob(logits: np.ndarray, targets: np.ndarray, active: Optional[np.
     if rc != 0:
         raise ValueError("unsupported shard count %d for V=%d" % (n_shards, V))
     return out
+
+
+def log_softmax(logits: np.ndarray, active: Optional[np.ndarray] = None):
+    """Contract log_softmax of fp32 logits [T, V] -> (out [T, V], lse [T])."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, V = L.shape
+    act = None if active is None else np.ascontiguousarray(active, dtype=np.uint8)
+    out = np.empty((T, V), np.float32)
+    lse = np.empty(T, np.float32)
+    rc = lib().emu_log_softmax(_ptr(L), T, V, _ptr(act), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("emu_log_softmax failed")
+    return out, lse
 
 
 def exp_sweep(lo: float, hi: float):

@@ -82,6 +82,16 @@ def lse_and_logprob_from_logits(L: np.ndarray, targets: np.ndarray,
     return lp, lse
 
 
+def log_softmax_from_logits(L: np.ndarray, active: Optional[np.ndarray] = None) -> np.ndarray:
+    """fp64 log_softmax l - lse of logits [T, V]; inactive rows -> 0."""
+    M = L.max(axis=1)
+    lse = M + np.log(np.exp(L - M[:, None]).sum(axis=1))
+    out = L - lse[:, None]
+    if active is not None:
+        out = np.where(np.asarray(active).astype(bool)[:, None], out, 0.0)
+    return out
+
+
 def selected_logprob(hidden_bits: np.ndarray, W_bits: np.ndarray, targets: np.ndarray,
                      active: Optional[np.ndarray] = None, rows: Optional[Sequence[int]] = None,
                      row_batch_bytes: int = 1 << 30) -> Tuple[np.ndarray, np.ndarray]:

@@ -115,3 +115,26 @@ def test_argument_validation_refuses_before_any_cuda_call(L):
     assert L.rlk_lse_merge(ctypes.cast(arr, ctypes.c_void_p), 3, 4, None, 0x40000, 0x50000, None,
                            None) == 2
     assert L.rlk_debug_logits(0x10000, 0x20000, 4, 100, 10, 0x40000, None, None) == 2
+
+
+def test_materialised_logits_validation(L):
+    f = L.rlk_logits_logprob
+    ok = dict(logits=0x10000, dtype=0, ld=1024, targets=0x30000, T=4, V=1000, n=1, lp=0x40000,
+              lse=0x50000, ws=0x60000, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["logits"], a["dtype"], a["ld"], a["targets"], None, a["T"], a["V"], a["n"],
+                 a["lp"], a["lse"], a["ws"], a["wsb"], None, None)
+    assert call(dtype=2) == 2
+    assert call(ld=999) == 1          # ld < V
+    assert call(logits=0x10002) == 3  # fp32 elements need 4-byte alignment
+    assert call(dtype=1, logits=0x10001) == 3  # bf16 elements need 2-byte alignment
+    assert call(V=0) == 1
+    assert call(n=3) == 2
+    assert call(targets=None) == 1
+    assert call(wsb=10) == 4
+    assert call(T=0) == 0
+    g = L.rlk_log_softmax
+    assert g(0x10000, 0, 1024, None, 4, 1000, None, 0x50000, 0x60000, 1 << 20, None, None) == 1
+    assert g(0x10001, 0, 1001, None, 4, 1000, 0x40000, 0x50000, 0x60000, 1 << 20, None, None) == 3
