@@ -286,6 +286,33 @@ int emu_log_softmax(const float* logits, int64_t T, int64_t V, const uint8_t* ac
     return 0;
 }
 
+/* fp32 -> bf16 bits, round to nearest even (finite inputs) */
+static uint16_t bf16_rne(float f) {
+    uint32_t u = f2u(f);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Gradient of sum_t g[t] logprob[t] with respect to the logits, as the
+ * backward's first stage writes it: p = rlk_exp(RN(l - lse)),
+ * d = RN(1 - p) at the target and -p elsewhere, G = bf16_RN(RN(g * d));
+ * inactive rows give +0.  lse is the forward's fp32 log-sum-exp.
+ */
+void emu_grad_logits(const float* logits, int64_t T, int64_t V, const float* lse,
+                     const int32_t* targets, const float* g, const uint8_t* active,
+                     uint16_t* out) {
+    for (int64_t t = 0; t < T; ++t) {
+        int act = active ? (active[t] != 0) : 1;
+        for (int64_t v = 0; v < V; ++v) {
+            if (!act) { out[t * V + v] = 0; continue; }
+            float p = emu_exp(logits[t * V + v] - lse[t]);
+            float d = (v == (int64_t)targets[t]) ? 1.0f - p : -p;
+            out[t * V + v] = bf16_rne(g[t] * d);
+        }
+    }
+}
+
 /* ---- exhaustive accuracy sweeps against fp64 libm (the independent reference) ---- */
 static double ulp_err(float y, double z) {
     if (z == 0.0) return y == 0.0f ? 0.0 : INFINITY;

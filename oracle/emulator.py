@@ -46,6 +46,8 @@ def lib():
             fn.argtypes = [f, f, P, P, P]
         L.emu_log_softmax.restype = i32
         L.emu_log_softmax.argtypes = [P, i64, i64, P, P, P]
+        L.emu_grad_logits.restype = None
+        L.emu_grad_logits.argtypes = [P, i64, i64, P, P, P, P, P]
         L.emu_constants.restype = None
         L.emu_constants.argtypes = [P]
         _lib = L
@@ -145,6 +147,19 @@ def log_softmax(logits: np.ndarray, active: Optional[np.ndarray] = None):
     if rc != 0:
         raise ValueError("emu_log_softmax failed")
     return out, lse
+
+
+def grad_logits(logits: np.ndarray, lse: np.ndarray, targets: np.ndarray, grad: np.ndarray,
+                active: Optional[np.ndarray] = None) -> np.ndarray:
+    """bf16 bits [T, V] of g * (onehot - exp(l - lse)) as the backward's first stage forms it."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, V = L.shape
+    out = np.empty((T, V), np.uint16)
+    act = None if active is None else np.ascontiguousarray(active, dtype=np.uint8)
+    lib().emu_grad_logits(_ptr(L), T, V, _ptr(np.ascontiguousarray(lse, np.float32)),
+                          _ptr(np.ascontiguousarray(targets, np.int32)),
+                          _ptr(np.ascontiguousarray(grad, np.float32)), _ptr(act), _ptr(out))
+    return out
 
 
 def exp_sweep(lo: float, hi: float):

@@ -166,3 +166,37 @@ def merge_partials(parts) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     tl = np.stack([p[2] for p in parts]).sum(axis=0)
     owners = np.stack([p[3] for p in parts]).astype(np.int64).sum(axis=0)
     return M + np.log(S), tl, owners
+
+
+# --------------------------------------------------------------------------
+# backward: gradients of sum_t g[t] * logprob[t]
+# --------------------------------------------------------------------------
+def grad_logits(L: np.ndarray, targets: np.ndarray, grad_logprob: np.ndarray,
+                active: Optional[np.ndarray] = None) -> np.ndarray:
+    """d/dl[t, v] of sum_t g[t] logprob[t] = g[t] (onehot(v = target[t]) - softmax(l[t])[v]).
+
+    The blog on bitwise consistency (sections 3.3, 4.2) asks the kernel for a
+    backward with the same numeric discipline as its forward; this is the
+    fp64 definition it is checked against.  Inactive rows give 0.
+    """
+    T, V = L.shape
+    M = L.max(axis=1)
+    lse = M + np.log(np.exp(L - M[:, None]).sum(axis=1))
+    P = np.exp(L - lse[:, None])
+    G = -P
+    tg = np.asarray(targets, dtype=np.int64)
+    ok = (tg >= 0) & (tg < V)
+    G[np.arange(T)[ok], tg[ok]] += 1.0
+    G *= np.asarray(grad_logprob, dtype=np.float64)[:, None]
+    if active is not None:
+        G[~np.asarray(active).astype(bool)] = 0.0
+    return G
+
+
+def backward(hidden_bits: np.ndarray, W_bits: np.ndarray, targets: np.ndarray,
+             grad_logprob: np.ndarray, active: Optional[np.ndarray] = None):
+    """fp64 (grad_hidden [T, H], grad_W [V, H]) of sum_t g[t] * logprob[t]."""
+    h = decode_bf16(hidden_bits)
+    Wd = decode_bf16(W_bits)
+    G = grad_logits(h @ Wd.T, targets, grad_logprob, active)
+    return G @ Wd, G.T @ h

@@ -178,6 +178,49 @@ def pin_tiny_regression(O):
     assert np.all(np.abs(lse - np.array(g["lse"])) <= 1e-12)
 
 
+def pin_backward_finite_differences(O):
+    """The analytic gradients against central differences of the oracle's own forward.
+
+    Perturbing one bf16 input and re-running the forward is an independent
+    route to the same derivative (the forward is pinned separately above).
+    Inputs are bf16 grid values; perturbations are done on the fp64 level by
+    evaluating the forward on exact fp64 inputs, so they need no bf16 step.
+    """
+    w = workloads.small_case(3, 8, 11, seed=16, w_std=0.5)
+    g = np.array([0.7, -1.3, 2.0])
+    h = O.decode_bf16(w.hidden)
+    Wd = O.decode_bf16(w.W)
+
+    def f(hh, WW):
+        lp, _ = O.lse_and_logprob_from_logits(hh @ WW.T, w.targets)
+        return float(np.dot(g, lp))
+
+    dh, dW = O.backward(w.hidden, w.W, w.targets, g)
+    eps = 1e-6
+    for (t, k) in [(0, 0), (1, 5), (2, 7)]:
+        hp, hm = h.copy(), h.copy()
+        hp[t, k] += eps
+        hm[t, k] -= eps
+        fd = (f(hp, Wd) - f(hm, Wd)) / (2 * eps)
+        assert abs(fd - dh[t, k]) <= 1e-6 * max(1.0, abs(fd)), (t, k, fd, dh[t, k])
+    for (v, k) in [(0, 0), (w.targets[1], 3), (10, 7)]:
+        Wp, Wm = Wd.copy(), Wd.copy()
+        Wp[v, k] += eps
+        Wm[v, k] -= eps
+        fd = (f(h, Wp) - f(h, Wm)) / (2 * eps)
+        assert abs(fd - dW[v, k]) <= 1e-6 * max(1.0, abs(fd)), (v, k, fd, dW[v, k])
+
+
+def pin_backward_rows_sum_to_zero(O):
+    """Each row of onehot - softmax sums to zero, so sum_v dlogit[t, v] = 0."""
+    w = workloads.small_case(5, 16, 300, seed=17)
+    L = O.logits(w.hidden, w.W)
+    G = O.grad_logits(L, w.targets, np.linspace(-2, 2, 5))
+    assert np.all(np.abs(G.sum(axis=1)) <= 1e-12)
+    assert np.all(G[np.arange(5), w.targets] * np.linspace(-2, 2, 5) >= 0)
+
+
 ALL_PINS = [pin_bf16_decode, pin_brute_force_tiny, pin_constant_logits, pin_two_class_softplus,
             pin_probabilities_sum_to_one, pin_shift_invariance, pin_shard_merge, pin_tile_tree,
-            pin_vocab_permutation, pin_masks_and_bad_targets]
+            pin_vocab_permutation, pin_masks_and_bad_targets, pin_backward_finite_differences,
+            pin_backward_rows_sum_to_zero]

@@ -118,9 +118,29 @@ def _mut_merge_unweighted(m):
     m.merge_partials = merge_partials
 
 
+def _mut_grad_sign(m):
+    orig = m.grad_logits
+    m.grad_logits = lambda L, targets, g, active=None: -orig(L, targets, g, active)
+
+
+def _mut_grad_unscaled(m):
+    orig = m.grad_logits
+    m.grad_logits = lambda L, targets, g, active=None: orig(L, targets, np.ones_like(g), active)
+
+
+def _mut_grad_transposed(m):
+    def backward(hidden_bits, W_bits, targets, grad_logprob, active=None):
+        h = m.decode_bf16(hidden_bits)
+        Wd = m.decode_bf16(W_bits)
+        G = m.grad_logits(h @ Wd.T, targets, grad_logprob, active)
+        return G @ Wd, (G.T @ h)[::-1]          # rows of grad_W in the wrong order
+    m.backward = backward
+
+
 MUTANTS = [_mut_decode_shift, _mut_k_reversed, _mut_drop_max, _mut_target_off_by_one,
            _mut_wrong_sign, _mut_exp_sign, _mut_dropped_term, _mut_mask_ignored,
-           _mut_floor_split, _mut_merge_unweighted]
+           _mut_floor_split, _mut_merge_unweighted, _mut_grad_sign, _mut_grad_unscaled,
+           _mut_grad_transposed]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
