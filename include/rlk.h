@@ -246,6 +246,36 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
                              int32_t* dev_status, rlk_stream_t stream);
 
 /*
+ * Backward of sum_t grad_logprob[t] * logprob[t] (the blog's requirement,
+ * sections 3.3 and 4.2, that the kernel provide a backward with the same
+ * numeric discipline as its forward):
+ *
+ *   G[t, v]        = bf16_RN(RN(g_t * d)), d = RN(1 - p) at the target, -p elsewhere,
+ *                    p = rlk_exp(RN(logit[t, v] - lse[t])), from the same fp32 logits
+ *   grad_hidden    = G · W   (fp32; the sum over v in 8 fixed ranges of ascending
+ *                    vocabulary, each one accumulator, added pairwise in fixed order;
+ *                    a token's row does not depend on the rest of the batch)
+ *   grad_W         = Gᵀ · h  (fp32; the sum over t ascending in one accumulator)
+ *
+ *   lse           device, float [T]: the forward's out_lse for this batch
+ *   grad_logprob  device, float [T]: dL/dlogprob
+ *   grad_hidden   device, float [T][H], or NULL to skip
+ *   grad_W        device, float [V][H], or NULL to skip (at least one is required)
+ *   workspace     >= rlk_backward_workspace_size(T, H, V) bytes, 256-byte aligned
+ *                 (holds G as bf16 [T][roundup(V, 8)] at offset 0)
+ * Inactive rows contribute nothing (their G row is zero).  An active row
+ * whose target lies outside [0, V) sets RLK_ERR_TARGET_RANGE and gets no
+ * one-hot term.  Other arguments as rlk_linear_logprob.
+ */
+size_t rlk_backward_workspace_size(int64_t T, int64_t H, int64_t V);
+rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
+                                         const int32_t* targets, const uint8_t* active_mask,
+                                         const float* grad_logprob, const float* lse, int64_t T,
+                                         int64_t H, int64_t V, float* grad_hidden, float* grad_W,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* dev_status, rlk_stream_t stream);
+
+/*
  * Same result as rlk_linear_logprob (same kernels, same bits), for callers
  * that cannot allocate device memory when they call: e.g. a rollout engine
  * that reserved almost all GPU memory for its KV cache at start-up, or a

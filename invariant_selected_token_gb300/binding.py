@@ -28,7 +28,8 @@ VOCAB_TILE = 128
 EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rlk_shard_range",
             "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
             "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
-            "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax"]
+            "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax",
+            "rlk_backward_workspace_size", "rlk_linear_logprob_backward"]
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 
@@ -74,6 +75,11 @@ def lib() -> ctypes.CDLL:
         L.rlk_debug_logits.argtypes = [P, P, i64, i64, i64, P, P, P]
         L.rlk_logits_logprob.restype = i32
         L.rlk_logits_logprob.argtypes = [P, i32, i64, P, P, i64, i64, i32, P, P, P, sz, P, P]
+        L.rlk_backward_workspace_size.restype = sz
+        L.rlk_backward_workspace_size.argtypes = [i64, i64, i64]
+        L.rlk_linear_logprob_backward.restype = i32
+        L.rlk_linear_logprob_backward.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, P, sz, P,
+                                                  P]
         L.rlk_log_softmax.restype = i32
         L.rlk_log_softmax.argtypes = [P, i32, i64, P, i64, i64, P, P, P, sz, P, P]
         _lib = L
@@ -308,3 +314,40 @@ def log_softmax(logits: torch.Tensor, active=None, out=None, out_lse=None, works
                                  _ptr(out), _ptr(out_lse), _ptr(workspace), workspace.numel(),
                                  _ptr(status), _stream(dev, stream)), "rlk_log_softmax")
     return out, out_lse
+
+
+def backward_workspace_size(T: int, H: int, V: int) -> int:
+    return int(lib().rlk_backward_workspace_size(T, H, V))
+
+
+def backward_grad_view(workspace: torch.Tensor, T: int, V: int) -> torch.Tensor:
+    """The bf16 logit gradient G [T, V] the backward leaves at the start of its workspace."""
+    ld = (V + 7) // 8 * 8
+    return workspace[:T * ld * 2].view(torch.bfloat16).view(T, ld)[:, :V]
+
+
+def linear_logprob_backward(hidden, W, targets, grad_logprob, lse, active=None,
+                            want_hidden: bool = True, want_W: bool = True, grad_hidden=None,
+                            grad_W=None, workspace=None, status=None, stream=None):
+    """(grad_hidden [T,H] or None, grad_W [V,H] or None) of sum_t g[t] * logprob[t]."""
+    dev = hidden.device
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W, torch.bfloat16, "W", dev, ndim=2)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    _require(grad_logprob, torch.float32, "grad_logprob", dev, ndim=1)
+    _require(lse, torch.float32, "lse", dev, ndim=1)
+    T, H = hidden.shape
+    V = W.shape[0]
+    if want_hidden and grad_hidden is None:
+        grad_hidden = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if want_W and grad_W is None:
+        grad_W = torch.empty((V, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(256, backward_workspace_size(T, H, V)), dtype=torch.uint8,
+                                device=dev)
+    _check(lib().rlk_linear_logprob_backward(
+        _ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), _ptr(grad_logprob), _ptr(lse), T, H, V,
+        _ptr(grad_hidden if want_hidden else None), _ptr(grad_W if want_W else None),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
+        "rlk_linear_logprob_backward")
+    return (grad_hidden if want_hidden else None), (grad_W if want_W else None)

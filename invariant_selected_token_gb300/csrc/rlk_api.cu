@@ -118,6 +118,7 @@ rlk_status_t device_check(DeviceState** out) {
         st.sm_count = sms;
         if (st.cc == 103) {
             if (rlk::prepare_tile_partials_kernels() != cudaSuccess) return RLK_ERR_CUDA;
+            if (rlk::prepare_gemm_kernels() != cudaSuccess) return RLK_ERR_CUDA;
         }
         if (!g_encode) {
             void* fn = nullptr;
@@ -176,10 +177,61 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     a.n_tiles = int(n_tiles_of(V_local));
     a.k_blocks = int(H / rlk::kBlockK);
     a.a_box_rows = a_rows;
-    return rlk::launch_tile_partials(map_h, map_w, a, dbg != nullptr, dev->sm_count, stream) ==
-                   cudaSuccess
+    a.lse = nullptr;
+    a.grad = nullptr;
+    a.G = nullptr;
+    a.ldG = 0;
+    a.V_total = V_local;
+    return rlk::launch_tile_partials(map_h, map_w, a,
+                                     dbg != nullptr ? rlk::kEpiDebugLogits : rlk::kEpiPartials,
+                                     dev->sm_count, stream) == cudaSuccess
                ? RLK_OK
                : RLK_ERR_CUDA;
+}
+
+// bf16 [rows][inner] row-major with row stride `stride_elems`, 64 x 64 boxes
+// (MN-major GEMM operands: the inner dimension is M or N, rows are K).
+rlk_status_t encode_bf16_mn_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                                int64_t stride_elems) {
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(stride_elems) * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_CUDA;
+}
+
+// K-major bf16 operand [rows][inner] with row stride `stride_elems`, boxes 64 x box_rows.
+rlk_status_t encode_bf16_k_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows,
+                               int64_t stride_elems, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(stride_elems) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(rlk::kBlockK), box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_CUDA;
+}
+
+constexpr int kGradHiddenSplits = 8;
+
+int64_t grad_ld(int64_t V) { return (V + 7) / 8 * 8; }
+
+struct BackwardLayout {
+    size_t G, parts, total;
+};
+
+BackwardLayout backward_layout_of(int64_t T, int64_t H, int64_t V) {
+    BackwardLayout l;
+    l.G = 0;
+    l.parts = align256(size_t(T) * size_t(grad_ld(V)) * 2);
+    l.total = l.parts + align256(size_t(kGradHiddenSplits) * size_t(T) * size_t(H) * 4);
+    return l;
 }
 
 rlk_status_t common_checks(const void* hidden, const void* W, const int32_t* targets, int64_t T,
@@ -483,6 +535,110 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
                                        int(V), out, dev->sm_count, st) == cudaSuccess
                ? RLK_OK
                : RLK_ERR_CUDA;
+}
+
+size_t rlk_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
+    if (T < 0 || H < rlk::kBlockK || H % rlk::kBlockK != 0 || V < 1 || V > RLK_MAX_VOCAB) return 0;
+    return backward_layout_of(T, H, V).total;
+}
+
+rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
+                                         const int32_t* targets, const uint8_t* active_mask,
+                                         const float* grad_logprob, const float* lse, int64_t T,
+                                         int64_t H, int64_t V, float* grad_hidden, float* grad_W,
+                                         void* workspace, size_t workspace_bytes,
+                                         int32_t* dev_status, rlk_stream_t stream) {
+    rlk_status_t s = common_checks(hidden, W, targets, T, H);
+    if (s != RLK_OK) return s;
+    if (V < 1) return RLK_ERR_INVALID_ARG;
+    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
+    if (T == 0) return RLK_OK;
+    if (!grad_logprob || !lse || !workspace || (!grad_hidden && !grad_W))
+        return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(grad_logprob, 4) || !aligned(lse, 4) ||
+        !aligned(grad_hidden, 4) || !aligned(grad_W, 4))
+        return RLK_ERR_ALIGNMENT;
+    const BackwardLayout l = backward_layout_of(T, H, V);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* G = reinterpret_cast<uint16_t*>(ws + l.G);
+    const int64_t ldG = grad_ld(V);
+
+    // 1. logits again, then G = g (onehot - softmax) in bf16 (the forward's lse)
+    CUtensorMap map_h, map_w;
+    const int a_rows = T >= kTileM ? kTileM : int((T + 7) / 8 * 8);
+    if ((s = encode_bf16_map(&map_h, hidden, H, T, uint32_t(a_rows))) != RLK_OK) return s;
+    if ((s = encode_bf16_map(&map_w, W, H, V, kTileN)) != RLK_OK) return s;
+    rlk::TilePartialsArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.targets = targets;
+    a.active = active_mask;
+    a.status = dev_status;
+    a.v_offset = 0;
+    a.T = int(T);
+    a.V_local = int(V);
+    a.n_tiles = int(n_tiles_of(V));
+    a.k_blocks = int(H / rlk::kBlockK);
+    a.a_box_rows = a_rows;
+    a.lse = lse;
+    a.grad = grad_logprob;
+    a.G = G;
+    a.ldG = ldG;
+    a.V_total = V;
+    if (rlk::launch_tile_partials(map_h, map_w, a, rlk::kEpiGrad, dev->sm_count, st) != cudaSuccess)
+        return RLK_ERR_CUDA;
+
+    // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum
+    if (grad_hidden) {
+        CUtensorMap map_g, map_wmn;
+        if ((s = encode_bf16_k_map(&map_g, G, V, T, ldG, kTileM)) != RLK_OK) return s;
+        if ((s = encode_bf16_mn_map(&map_wmn, W, H, V, H)) != RLK_OK) return s;
+        const int kb = int((V + rlk::kBlockK - 1) / rlk::kBlockK);
+        const int splits = kb < kGradHiddenSplits ? kb : kGradHiddenSplits;
+        rlk::GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.out = reinterpret_cast<float*>(ws + l.parts);
+        g.ld_out = H;
+        g.split_stride = T * H;
+        g.M = int(T);
+        g.N = int(H);
+        g.k_blocks = kb;
+        g.kb_per_split = (kb + splits - 1) / splits;
+        g.splits = (kb + g.kb_per_split - 1) / g.kb_per_split;
+        g.vec_store = true;
+        g.status = dev_status;
+        if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+        if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
+                                   dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+    }
+
+    // 3. grad_W = G^T h: K = T ascending, one range
+    if (grad_W) {
+        CUtensorMap map_gt, map_hmn;
+        if ((s = encode_bf16_mn_map(&map_gt, G, V, T, ldG)) != RLK_OK) return s;
+        if ((s = encode_bf16_mn_map(&map_hmn, hidden, H, T, H)) != RLK_OK) return s;
+        rlk::GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.out = grad_W;
+        g.ld_out = H;
+        g.split_stride = 0;
+        g.M = int(V);
+        g.N = int(H);
+        g.k_blocks = int((T + rlk::kBlockK - 1) / rlk::kBlockK);
+        g.kb_per_split = g.k_blocks;
+        g.splits = 1;
+        g.vec_store = aligned(grad_W, 16);
+        g.n_fastest = true;
+        g.status = dev_status;
+        if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
 }
 
 }  // extern "C"

@@ -30,11 +30,19 @@ struct TilePartialsArgs {
     int n_tiles;              // ceil(V_local / 128): row stride of partials
     int k_blocks;             // H / 64
     int a_box_rows;           // rows of the hidden TMA box: 128, or roundup(T, 8) when T <= 128
+    // backward (gradient epilogue) only
+    const float* lse;         // [T] forward log-sum-exp
+    const float* grad;        // [T] dL/dlogprob
+    uint16_t* G;              // bf16 [T][ldG] logit gradient
+    int64_t ldG;
+    int64_t V_total;          // for the target-range check
 };
+
+enum TileEpilogue { kEpiPartials = 0, kEpiDebugLogits = 1, kEpiGrad = 2 };
 
 // hidden map: bf16 [T][H], box 64 x 128; weight map: bf16 [V_local][H], box 64 x 256.
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                                 const TilePartialsArgs& a, bool debug_logits, int num_sms,
+                                 const TilePartialsArgs& a, int epilogue, int num_sms,
                                  cudaStream_t stream);
 int tile_partials_smem_bytes();
 cudaError_t prepare_tile_partials_kernels();
@@ -71,6 +79,26 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
 cudaError_t launch_log_softmax_out(const void* logits, int dtype, int64_t ld, const float* lse,
                                    const uint8_t* active, int T, int V, float* out, int num_sms,
                                    cudaStream_t stream);
+
+struct GemmArgs {
+    float* out;               // [splits][M][ld_out] fp32
+    int64_t ld_out;
+    int64_t split_stride;     // elements between split partials
+    int M, N;
+    int k_blocks;             // ceil(K / 64)
+    int kb_per_split;
+    int splits;
+    bool vec_store;           // out rows 16-byte aligned
+    bool n_fastest;           // raster: N tiles fastest (CTAs side by side share the A slice)
+    int32_t* status;
+};
+
+// A MN-major or K-major, B MN-major; 128 x 256 tiles, fixed K ranges per split.
+cudaError_t launch_gemm_f32(const CUtensorMap& map_a, const CUtensorMap& map_b, bool a_mn,
+                            bool b_mn, const GemmArgs& g, int num_sms, cudaStream_t stream);
+cudaError_t prepare_gemm_kernels();
+cudaError_t launch_sum_splits(const float* parts, int64_t split_stride, int splits, int64_t n,
+                              float* out, int num_sms, cudaStream_t stream);
 
 struct ShardMergeArgs {
     const rlk_partial_t* parts[RLK_MAX_SHARDS];

@@ -23,6 +23,7 @@
 // T, the row position or the launch shape, so the per-tile values depend on
 // the token and the tile only.  There is no split over K on any path.
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -81,7 +82,43 @@ __device__ __forceinline__ MaxSum reduce_tile(float (&v)[kVocabTile], int ncols)
     return r;
 }
 
-template <bool kDebug>
+// Backward epilogue: G[t, c] = bf16_RN(RN(g_t * d)) with d = RN(1 - p) at the
+// target and -p elsewhere, p = rlk_exp(RN(l - lse_t)) -- the gradient of
+// g_t * logprob_t with respect to the logits, from the same fp32 logits and
+// the same exp the forward used.  Inactive rows write zeros.
+__device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const TilePartialsArgs& a,
+                                          int t, int c0, int ncols, bool valid, int64_t tl) {
+    const float lse = valid ? a.lse[t] : 0.0f;
+    const float gt = valid ? a.grad[t] : 0.0f;
+    uint16_t* dst = a.G + static_cast<int64_t>(t) * a.ldG + c0;
+#pragma unroll
+    for (int q = 0; q < kVocabTile / 8; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            uint32_t pair = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int c = q * 8 + i + h;
+                const float p = contract_exp(__fsub_rn(v[c], lse));
+                const float d = (c == tl) ? __fsub_rn(1.0f, p) : -p;
+                const float gv = valid ? __fmul_rn(gt, d) : 0.0f;
+                const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(gv));
+                pair |= b << (16 * h);
+            }
+            w[i / 2] = pair;
+        }
+        if (q * 8 + 8 <= ncols) {
+            *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (q * 8 + i < ncols) dst[q * 8 + i] = static_cast<uint16_t>(w[i / 2] >> (16 * (i & 1)));
+        }
+    }
+}
+
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
                     const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
@@ -218,8 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool valid = t < a.T;
             if (valid && a.active) valid = a.active[t] != 0;
             const int64_t tg_local =
-                (!kDebug && valid) ? static_cast<int64_t>(a.targets[t]) - a.v_offset : -1;
-            if (__any_sync(0xffffffffu, kDebug ? (t < a.T) : valid)) {
+                (kEpi != kEpiDebugLogits && valid) ? static_cast<int64_t>(a.targets[t]) - a.v_offset
+                                                   : -1;
+            if (kEpi == kEpiGrad && valid && n_blk == 0 && (tg_local < 0 || tg_local >= a.V_total))
+                report(a.status, RLK_ERR_TARGET_RANGE);
+            if (__any_sync(0xffffffffu, kEpi == kEpiPartials ? valid : (t < a.T))) {
 #pragma unroll 1
                 for (int sub = 0; sub < kTileN / kVocabTile; ++sub) {
                     const int j = n_blk * (kTileN / kVocabTile) + sub;
@@ -237,11 +277,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[q * 32 + i] = part[i];
                     }
-                    if (kDebug) {
+                    if (kEpi == kEpiDebugLogits) {
                         if (t < a.T) {
                             float* dst = a.dbg_logits + static_cast<int64_t>(t) * a.V_local + c0;
                             for (int c = 0; c < ncols; ++c) dst[c] = v[c];
                         }
+                        continue;
+                    }
+                    if (kEpi == kEpiGrad) {
+                        if (t < a.T) grad_tile(v, a, t, c0, ncols, valid, tg_local - c0);
                         continue;
                     }
                     const int64_t tl = tg_local - c0;
@@ -289,24 +333,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 int tile_partials_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prepare_tile_partials_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<false>,
+    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<kEpiPartials>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_tile_partials<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes);
+    e = cudaFuncSetAttribute(k_tile_partials<kEpiDebugLogits>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_tile_partials<kEpiGrad>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                                 const TilePartialsArgs& a, bool debug_logits, int num_sms,
+                                 const TilePartialsArgs& a, int epilogue, int num_sms,
                                  cudaStream_t stream) {
     const int num_m = (a.T + kTileM - 1) / kTileM;
     const int num_n = (a.V_local + kTileN - 1) / kTileN;
     const int64_t total = static_cast<int64_t>(num_m) * num_n;
     const int grid = static_cast<int>(total < num_sms ? total : num_sms);
-    if (debug_logits)
-        k_tile_partials<true><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+    if (epilogue == kEpiDebugLogits)
+        k_tile_partials<kEpiDebugLogits><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+    else if (epilogue == kEpiGrad)
+        k_tile_partials<kEpiGrad><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
     else
-        k_tile_partials<false><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+        k_tile_partials<kEpiPartials><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
     return cudaGetLastError();
 }
 
