@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode256",
-                            "logits_fp32", "logits_bf16"],
+                            "logits_fp32", "logits_bf16", "backward"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path")
@@ -302,6 +302,65 @@ def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
     return 0
 
 
+def backward_arm(args, rank, world, dev, dist, W, pk, binding):
+    """grad_hidden and grad_W of sum_t g[t] logprob[t] for the packed batch."""
+    import torch
+    T = pk.hidden.shape[0]
+    _, lse = binding.linear_logprob(pk.hidden, W, pk.targets, None, N_SHARDS)
+    g = torch.randn(T, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    ws = torch.empty(binding.backward_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.linear_logprob_backward(pk.hidden, W, pk.targets, g, lse, None, True, True, dh, dW,
+                                        ws, status, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status)
+    K = max(1, args.steps // 4)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index or 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    s0.record(stream)
+    for _ in range(K):
+        step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(t0, time.time())
+    ms_total = max_over_ranks(s0.elapsed_time(s1), dist, dev)
+    ms = ms_total / K
+    flops = 3 * 2.0 * T * H * V  # logits again, grad_hidden, grad_W
+    peaks = load_peaks()
+    achieved = flops / (ms / 1000.0) / 1e12
+    if rank == 0:
+        out = {"metric": METRIC.replace("selected-logprob", "selected-logprob backward"),
+               "value": weak_scaling_value(world, T, K, ms_total), "unit": "tokens/s",
+               "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+               "data": "synthetic",
+               "config": {"workload": "backward of the packed batch (T=4096, H=4096, V=151936): "
+                                      "grad_hidden and grad_W", "T": T, "H": H, "V": V},
+               "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                            "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                            "kernel": "whole backward call (gradient epilogue + 2 GEMMs + split sum)",
+                            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
+               "cpu_baseline": None, "e2e": None, "gpu_launches": 4 * K, "clocks": clk,
+               "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out))
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -342,6 +401,8 @@ def main():
                     "4 vocab shards" % n)
     if args.workload.startswith("logits_"):
         return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
+    if args.workload == "backward":
+        return backward_arm(args, rank, world, dev, dist, W, pk, binding)
     T = hidden.shape[0]
     ws = binding.new_workspace(T, V, N_SHARDS, dev)
     out_lp = torch.empty(T, dtype=torch.float32, device=dev)

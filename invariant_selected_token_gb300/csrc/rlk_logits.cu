@@ -118,7 +118,13 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
     }
 }
 
-template <int kEpi>
+// kPair: CTAs run in clusters of two along the token dimension.  Both CTAs of
+// a cluster work on the same W slice (token tiles 2p and 2p+1): each loads
+// its own hidden tile and one half (128 rows) of the W tile, multicast into
+// both CTAs' shared memory, so each W byte crosses L2 once per pair.  Each
+// CTA still issues its own M=128, N=256 MMAs on the full W tile, so the
+// arithmetic -- and every bit -- is that of the unpaired kernel.
+template <int kEpi, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
                     const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
@@ -138,12 +144,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int num_m = (a.T + kTileM - 1) / kTileM;
     const int num_n = (a.V_local + kTileN - 1) / kTileN;
-    const int total = num_m * num_n;
+    // a work unit is one W tile and one token tile (kPair: a pair of token tiles)
+    const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+    const int num_mu = kPair ? (num_m + 1) / 2 : num_m;
+    const int total = num_mu * num_n;
+    const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int ustride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            // kPair: a stage is free once both CTAs' MMAs have read it
+            ptx::mbar_init(&empty[s], kPair ? 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -160,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any multicast
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -170,9 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // hidden rows; the accumulator rows beyond them are never read.
             const uint32_t a_bytes = static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2;
             uint32_t stage = 0, phase = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-                const int n_blk = tile / num_m;
-                const int m_blk = tile - n_blk * num_m;
+            for (int unit = unit0; unit < total && !*abort_flag; unit += ustride) {
+                const int n_blk = unit / num_mu;
+                const int m_blk = kPair ? 2 * (unit - n_blk * num_mu) + static_cast<int>(rank)
+                                        : unit - n_blk * num_mu;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         *abort_flag = 1;
@@ -182,8 +196,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[stage], a_bytes + kStageBytesB);
                     ptx::tma_load_2d(sA + stage * kStageBytesA, &map_hidden, &full[stage],
                                      kb * kBlockK, m_blk * kTileM);
-                    ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
-                                     kb * kBlockK, n_blk * kTileN);
+                    if (kPair) {
+                        // this CTA's half of the W tile, into both CTAs
+                        ptx::tma_load_2d_multicast(sB + stage * kStageBytesB + rank * (kStageBytesB / 2),
+                                                   &map_w, &full[stage], kb * kBlockK,
+                                                   n_blk * kTileN + static_cast<int>(rank) * (kTileN / 2),
+                                                   static_cast<uint16_t>(0x3));
+                    } else {
+                        ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
+                                         kb * kBlockK, n_blk * kTileN);
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -195,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ---------------- MMA issuer
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-            for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+            for (int unit = unit0; unit < total && !*abort_flag; unit += ustride) {
                 if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     report(a.status, RLK_ERR_TIMEOUT);
@@ -219,7 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ptx::smem_desc_k_sw128(b0 + kk * 32), kIdesc,
                                       (kb | kk) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(&empty[stage]);
+                    if (kPair)
+                        ptx::mma_commit_multicast(&empty[stage], static_cast<uint16_t>(0x3));
+                    else
+                        ptx::mma_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -242,9 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const int n_blk = tile / num_m;
-            const int m_blk = tile - n_blk * num_m;
+        for (int unit = unit0; unit < total; unit += ustride) {
+            const int n_blk = unit / num_mu;
+            const int m_blk = kPair ? 2 * (unit - n_blk * num_mu) + static_cast<int>(rank)
+                                    : unit - n_blk * num_mu;
             if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) {
                 *abort_flag = 1;
                 report(a.status, RLK_ERR_TIMEOUT);
@@ -321,6 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
+    // kPair: neither CTA leaves while the other may still multicast into it
+    // or arrive on its barriers
+    if (kPair) ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
@@ -328,35 +357,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int kEpi>
+cudaError_t set_smem_attr() {
+    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<kEpi, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_tile_partials<kEpi, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+// Clusters of two CTAs that fit at once on this device (0 if none).
+int max_pair_clusters() {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_tile_partials<kEpiPartials, true>, &cfg) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+template <int kEpi>
+cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
+                       const TilePartialsArgs& a, bool pair, int num_sms, int pair_clusters,
+                       cudaStream_t stream) {
+    const int num_m = (a.T + kTileM - 1) / kTileM;
+    const int num_n = (a.V_local + kTileN - 1) / kTileN;
+    if (!pair) {
+        const int64_t total = static_cast<int64_t>(num_m) * num_n;
+        const int grid = static_cast<int>(total < num_sms ? total : num_sms);
+        k_tile_partials<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
+        return cudaGetLastError();
+    }
+    const int64_t units = static_cast<int64_t>((num_m + 1) / 2) * num_n;
+    const int clusters = static_cast<int>(units < pair_clusters ? units : pair_clusters);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, true>, map_hidden, map_w, a);
+}
+
 }  // namespace
 
 int tile_partials_smem_bytes() { return kSmemBytes; }
 
-cudaError_t prepare_tile_partials_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<kEpiPartials>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_tile_partials<kEpiDebugLogits>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_tile_partials<kEpiGrad>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+cudaError_t prepare_tile_partials_kernels(int* pair_clusters) {
+    cudaError_t e;
+    if ((e = set_smem_attr<kEpiPartials>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<kEpiDebugLogits>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<kEpiGrad>()) != cudaSuccess) return e;
+    *pair_clusters = max_pair_clusters();
+    return cudaSuccess;
 }
 
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                                 const TilePartialsArgs& a, int epilogue, int num_sms,
-                                 cudaStream_t stream) {
-    const int num_m = (a.T + kTileM - 1) / kTileM;
-    const int num_n = (a.V_local + kTileN - 1) / kTileN;
-    const int64_t total = static_cast<int64_t>(num_m) * num_n;
-    const int grid = static_cast<int>(total < num_sms ? total : num_sms);
+                                 const TilePartialsArgs& a, int epilogue, bool pair, int num_sms,
+                                 int pair_clusters, cudaStream_t stream) {
     if (epilogue == kEpiDebugLogits)
-        k_tile_partials<kEpiDebugLogits><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
-    else if (epilogue == kEpiGrad)
-        k_tile_partials<kEpiGrad><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
-    else
-        k_tile_partials<kEpiPartials><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
-    return cudaGetLastError();
+        return launch_epi<kEpiDebugLogits>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
+    if (epilogue == kEpiGrad)
+        return launch_epi<kEpiGrad>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
+    return launch_epi<kEpiPartials>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
 }
 
 }  // namespace rlk
