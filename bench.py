@@ -390,6 +390,10 @@ def main():
 
     W = WL.head_weights(dev)                       # same weights on every rank
     pk = WL.packed(W, dev, seed=rank_batch_seed(rank))  # each rank its own batch
+    if args.workload.startswith("logits_"):
+        return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
+    if args.workload == "backward":
+        return backward_arm(args, rank, world, dev, dist, W, pk, binding)
     if args.workload == "packed":
         hidden, targets = pk.hidden, pk.targets
         workload = WORKLOAD
@@ -399,10 +403,6 @@ def main():
         hidden, targets = pk.hidden[idx].contiguous(), pk.targets[idx].contiguous()
         workload = ("decode batch T=%d (rows of the packed batch), H=4096, V=151936, bf16, "
                     "4 vocab shards" % n)
-    if args.workload.startswith("logits_"):
-        return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
-    if args.workload == "backward":
-        return backward_arm(args, rank, world, dev, dist, W, pk, binding)
     T = hidden.shape[0]
     ws = binding.new_workspace(T, V, N_SHARDS, dev)
     out_lp = torch.empty(T, dtype=torch.float32, device=dev)

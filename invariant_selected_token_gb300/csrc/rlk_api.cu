@@ -157,10 +157,20 @@ rlk_status_t encode_bf16_map(CUtensorMap* map, const void* base, int64_t inner, 
 // Paired (2-CTA cluster, W tile multicast) schedule for batches of more than
 // one token tile.  Both schedules issue the same MMAs per logit, so the
 // choice never changes a bit; RLK_TEST_PAIR=0|1 forces one (tests use it).
+// Measured on GB300 the paired schedule is no faster (the two CTAs of a pair
+// run in lockstep), so it is off unless RLK_TEST_PAIR=1 asks for it.
 bool use_pair(int64_t T, const DeviceState* dev) {
-    bool pair = T > kTileM && dev->pair_clusters >= 1;
-    if (const char* f = std::getenv("RLK_TEST_PAIR")) pair = std::atoi(f) != 0 && dev->pair_clusters >= 1;
-    return pair;
+    bool pair = false;
+    if (const char* f = std::getenv("RLK_TEST_PAIR")) pair = std::atoi(f) != 0;
+    return pair && T > kTileM && dev->pair_clusters >= 1;
+}
+
+// RLK_TEST_DROP_STAGE=1: CTA 0's producer skips its first pipeline stage, so
+// its MMA wait runs out (bounded) and the kernel reports RLK_ERR_TIMEOUT --
+// the failure-detection test's way to exercise the give-up path.
+bool test_drop_stage() {
+    const char* f = std::getenv("RLK_TEST_DROP_STAGE");
+    return f && std::atoi(f) != 0;
 }
 
 rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t* targets,
@@ -189,6 +199,7 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     a.n_tiles = int(n_tiles_of(V_local));
     a.k_blocks = int(H / rlk::kBlockK);
     a.a_box_rows = a_rows;
+    a.test_drop_stage = test_drop_stage() ? 1 : 0;
     a.lse = nullptr;
     a.grad = nullptr;
     a.G = nullptr;

@@ -30,6 +30,7 @@ struct TilePartialsArgs {
     int n_tiles;              // ceil(V_local / 128): row stride of partials
     int k_blocks;             // H / 64
     int a_box_rows;           // rows of the hidden TMA box: 128, or roundup(T, 8) when T <= 128
+    int test_drop_stage;      // test only: CTA 0 never loads its first stage (wait runs out)
     // backward (gradient epilogue) only
     const float* lse;         // [T] forward log-sum-exp
     const float* grad;        // [T] dL/dlogprob

@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // hidden rows; the accumulator rows beyond them are never read.
             const uint32_t a_bytes = static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2;
             uint32_t stage = 0, phase = 0;
+            if (a.test_drop_stage && blockIdx.x == 0) {
+                // test only: leave stage 0 unfilled; the MMA's bounded wait gives up
+                stage = 1;
+            }
             for (int unit = unit0; unit < total && !*abort_flag; unit += ustride) {
                 const int n_blk = unit / num_mu;
                 const int m_blk = kPair ? 2 * (unit - n_blk * num_mu) + static_cast<int>(rank)

@@ -86,3 +86,28 @@ def test_unaligned_hidden_refused(rlk, cuda_device):
     with pytest.raises(rlk.RlkError) as e:
         rlk.linear_logprob(h, W, t)
     assert e.value.code == 3
+
+
+def test_pipeline_wait_gives_up_with_timeout_status(rlk, cuda_device, monkeypatch):
+    """A pipeline stage that never fills: the bounded wait gives up, the kernel reports
+    RLK_ERR_TIMEOUT and returns, and the context stays usable for the next call."""
+    import time
+    w = WL.small_case(64, 256, 1024, seed=12)
+    dw = WL.to_device(w, cuda_device)
+    monkeypatch.setenv("RLK_TEST_DROP_STAGE", "1")
+    status = rlk.new_status(cuda_device)
+    t0 = time.time()
+    rlk.linear_logprob(dw.hidden, dw.W, dw.targets, None, 1, status=status)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    monkeypatch.delenv("RLK_TEST_DROP_STAGE")
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.raise_on_device_status(status)
+    assert e.value.code == rlk.RLK_ERR_TIMEOUT
+    assert elapsed < 30
+    status2 = rlk.new_status(cuda_device)
+    lp, _ = rlk.linear_logprob(dw.hidden, dw.W, dw.targets, None, 1, status=status2)
+    torch.cuda.synchronize()
+    rlk.raise_on_device_status(status2)
+    ref_lp, _ = O.selected_logprob(w.hidden, w.W, w.targets)
+    assert np.abs(lp.cpu().numpy() - ref_lp).max() <= 1e-4
