@@ -121,6 +121,7 @@ rlk_status_t device_check(DeviceState** out) {
             if (rlk::prepare_tile_partials_kernels(&st.pair_clusters) != cudaSuccess)
                 return RLK_ERR_CUDA;
             if (rlk::prepare_gemm_kernels() != cudaSuccess) return RLK_ERR_CUDA;
+            if (rlk::prepare_mat_kernels() != cudaSuccess) return RLK_ERR_CUDA;
         }
         if (!g_encode) {
             void* fn = nullptr;

@@ -79,6 +79,7 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
                                      const int32_t* targets, const uint8_t* active, int T, int V,
                                      float2* partials, float* tgt_logit, int num_sms,
                                      cudaStream_t stream);
+cudaError_t prepare_mat_kernels();
 // out[t][v] = RN(l[t][v] - lse[t])
 cudaError_t launch_log_softmax_out(const void* logits, int dtype, int64_t ld, const float* lse,
                                    const uint8_t* active, int T, int V, float* out, int num_sms,

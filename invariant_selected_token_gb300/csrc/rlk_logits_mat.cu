@@ -6,14 +6,13 @@
 // reduction tree, fp32 accumulation).  These kernels apply the same numeric
 // contract as the fused path to a [T, V] fp32 or bf16 logits matrix:
 //
-//   k_mat_tile_partials  a warp per run of (token, 128-column tile)s: lane l holds
-//                        columns 4l..4l+3; the pairwise tree over the column
-//                        index is levels 1-2 inside the lane and levels 3-7
-//                        across lanes (xor 1, 2, 4, 8, 16; lower lane left),
-//                        which is exactly the contract's 128-slot tree.  The
-//                        (m, s) pairs and the target logit go to the same
-//                        workspace layout the fused path uses, so the tile
-//                        tree kernel finishes the job unchanged.
+//   k_mat_tile_partials  a warp stages 32 tiles of one row in shared memory,
+//                        then each lane reduces one whole 128-column tile in
+//                        registers with the contract's in-tile pairwise tree
+//                        (the fused epilogue's own arithmetic).  The (m, s)
+//                        pairs and the target logit go to the same workspace
+//                        layout the fused path uses, so the tile tree kernel
+//                        finishes the job unchanged.
 //   k_log_softmax_out    out[t, v] = RN(l[t, v] - lse[t]).
 //
 // Given the fused path's own fp32 logits, this path returns the fused path's
@@ -30,7 +29,7 @@
 namespace rlk {
 namespace {
 
-constexpr int kMatWarps = 8;
+constexpr int kMatWarps = 4;
 
 // Four consecutive logits of one row as fp32 (bf16 widens exactly).  Columns
 // at or beyond `ncols` read as -inf (they are not part of the tile).
@@ -65,69 +64,143 @@ __device__ __forceinline__ void load4(const void* row, int64_t c0, int ncols, in
     }
 }
 
-// (m, s) of one 128-column tile held 4 columns per lane, plus the target pick.
+// Thread-per-tile reduction from shared memory.  A warp stages a slice of
+// one row -- 32 consecutive 128-column tiles -- with coalesced loads into
+// shared memory (tile i at a 132-float pitch, so the later per-thread reads
+// are free of bank conflicts), then lane i reduces tile i in registers with
+// the contract's in-tile pairwise tree, exactly as the fused path's epilogue
+// does.  No cross-lane reduction remains.
+constexpr int kSliceTiles = 32;
+// Staged tile pitch in elements: a multiple of 16 bytes (16-byte copies and
+// reads stay aligned) that is an odd number of 16-byte chunks (consecutive
+// lanes' 16-byte reads fall in different bank groups): 132 fp32 = 33 chunks,
+// 136 bf16 = 17 chunks.
 template <int kDtype>
-__device__ __forceinline__ float2 tile_pair(const float (&x)[4], int lane) {
-    float m = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // levels 1-2 of the 128-slot tree inside the lane (padding gives exp(-inf) = +0)
-    const float e0 = contract_exp(__fsub_rn(x[0], m));
-    const float e1 = contract_exp(__fsub_rn(x[1], m));
-    const float e2 = contract_exp(__fsub_rn(x[2], m));
-    const float e3 = contract_exp(__fsub_rn(x[3], m));
-    float s = __fadd_rn(__fadd_rn(e0, e1), __fadd_rn(e2, e3));
-    // levels 3-7 across lanes, the lower lane's partial on the left
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const float other = __shfl_xor_sync(0xffffffffu, s, o);
-        s = (lane & o) ? __fadd_rn(other, s) : __fadd_rn(s, other);
+struct Pitch {
+    static constexpr int value = kDtype == RLK_DTYPE_F32 ? kVocabTile + 4 : kVocabTile + 8;
+};
+
+// Copy the slice's real columns into shared memory in their input type
+// (element e of the slice at tile e/128, column e%128, tile pitch kPitch
+// elements).  Aligned rows use asynchronous 16-byte copies, all in flight
+// at once; a row tail or an unaligned row falls back to plain loads.
+template <int kDtype>
+__device__ __forceinline__ void stage_slice(const void* row, int64_t c0, int ncols_total, int lane,
+                                            bool vec, void* sm_raw) {
+    constexpr int kElem = kDtype == RLK_DTYPE_F32 ? 4 : 2;
+    constexpr int kPitch = Pitch<kDtype>::value;
+    constexpr int kPerChunk = 16 / kElem;  // elements per 16-byte copy
+    const uint8_t* src = static_cast<const uint8_t*>(row) + c0 * kElem;
+    uint8_t* sm = static_cast<uint8_t*>(sm_raw);
+    const int full_chunks = vec ? ncols_total / kPerChunk : 0;
+    for (int ch = lane; ch < full_chunks; ch += 32) {
+        const int e = ch * kPerChunk;
+        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(
+            sm + ((e / kVocabTile) * kPitch + e % kVocabTile) * kElem));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + e * kElem)
+                     : "memory");
     }
-    return make_float2(m, s);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    for (int e = full_chunks * kPerChunk + lane; e < ncols_total; e += 32) {
+        uint8_t* d = sm + ((e / kVocabTile) * kPitch + e % kVocabTile) * kElem;
+        if (kDtype == RLK_DTYPE_F32)
+            *reinterpret_cast<float*>(d) = reinterpret_cast<const float*>(src)[e];
+        else
+            *reinterpret_cast<uint16_t*>(d) = reinterpret_cast<const uint16_t*>(src)[e];
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Warps walk runs of kRun consecutive tiles of one row (no per-tile index
-// division), two tiles in flight per step.
+// Element c of a staged tile as fp32 (bf16 widens exactly).
+template <int kDtype>
+__device__ __forceinline__ void read_tile(const void* sm_raw, int tile, float (&v)[kVocabTile]) {
+    constexpr int kPitch = Pitch<kDtype>::value;
+    if (kDtype == RLK_DTYPE_F32) {
+        const float* p = static_cast<const float*>(sm_raw) + tile * kPitch;
+#pragma unroll
+        for (int c = 0; c < kVocabTile; c += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(p + c);
+            v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
+        }
+    } else {
+        const uint16_t* p = static_cast<const uint16_t*>(sm_raw) + tile * kPitch;
+#pragma unroll
+        for (int c = 0; c < kVocabTile; c += 8) {
+            const uint4 q = *reinterpret_cast<const uint4*>(p + c);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[c + 2 * i] = __uint_as_float(w[i] << 16);
+                v[c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+    }
+}
+
 template <int kDtype>
 __global__ void __launch_bounds__(kMatWarps * 32)
     k_mat_tile_partials(const void* logits, int64_t ld, bool vec, const int32_t* targets,
                         const uint8_t* active, int T, int V, int n_tiles, float2* partials,
                         float* tgt_logit) {
-    constexpr int kRun = 16;
+    extern __shared__ float4 mat_smem[];
     const int lane = threadIdx.x & 31;
-    const int runs_per_row = (n_tiles + kRun - 1) / kRun;
-    const int64_t n_runs = static_cast<int64_t>(T) * runs_per_row;
+    const int warp = threadIdx.x >> 5;
+    constexpr int kElem = kDtype == RLK_DTYPE_F32 ? 4 : 2;
+    void* sm = reinterpret_cast<uint8_t*>(mat_smem) +
+               warp * (kSliceTiles * Pitch<kDtype>::value * kElem);
+    const int slices_per_row = (n_tiles + kSliceTiles - 1) / kSliceTiles;
+    const int64_t n_tasks = static_cast<int64_t>(T) * slices_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kMatWarps;
     const int elem = kDtype == RLK_DTYPE_F32 ? 4 : 2;
-    for (int64_t run = static_cast<int64_t>(blockIdx.x) * kMatWarps + (threadIdx.x >> 5);
-         run < n_runs; run += stride) {
-        const int t = static_cast<int>(run / runs_per_row);
-        const int j0 = static_cast<int>(run - static_cast<int64_t>(t) * runs_per_row) * kRun;
+    for (int64_t task = static_cast<int64_t>(blockIdx.x) * kMatWarps + warp; task < n_tasks;
+         task += stride) {
+        const int t = static_cast<int>(task / slices_per_row);
+        const int j0 = static_cast<int>(task - static_cast<int64_t>(t) * slices_per_row) * kSliceTiles;
         if (active && active[t] == 0) continue;
-        const int j1 = min(n_tiles, j0 + kRun);
+        const int64_t c0 = static_cast<int64_t>(j0) * kVocabTile;
+        const int ncols_total = min(kSliceTiles * kVocabTile, V - static_cast<int>(c0));
         const void* row = static_cast<const uint8_t*>(logits) + static_cast<int64_t>(t) * ld * elem;
-        const int64_t tg = targets ? static_cast<int64_t>(targets[t]) : -1;
-        float2* prow = partials + static_cast<int64_t>(t) * n_tiles;
-        for (int j = j0; j < j1; j += 2) {
-            const bool two = j + 1 < j1;
-            const int64_t c0 = static_cast<int64_t>(j) * kVocabTile;
-            const int nc0 = min(kVocabTile, V - static_cast<int>(c0));
-            const int nc1 = two ? min(kVocabTile, V - static_cast<int>(c0) - kVocabTile) : 0;
-            float x[4], y[4];
-            load4<kDtype>(row, c0, nc0, lane, vec, x);
-            if (two) load4<kDtype>(row, c0 + kVocabTile, nc1, lane, vec, y);
-            const int64_t tl = tg - c0 - 4 * lane;
-            if (tl >= 0 && tl < 4 && 4 * lane + tl < nc0)
-                tgt_logit[t] = tl == 0 ? x[0] : tl == 1 ? x[1] : tl == 2 ? x[2] : x[3];
-            const float2 p0 = tile_pair<kDtype>(x, lane);
-            if (lane == 0) prow[j] = p0;
-            if (two) {
-                const int64_t tl1 = tl - kVocabTile;
-                if (tl1 >= 0 && tl1 < 4 && 4 * lane + tl1 < nc1)
-                    tgt_logit[t] = tl1 == 0 ? y[0] : tl1 == 1 ? y[1] : tl1 == 2 ? y[2] : y[3];
-                const float2 p1 = tile_pair<kDtype>(y, lane);
-                if (lane == 0) prow[j + 1] = p1;
+        __syncwarp();
+        stage_slice<kDtype>(row, c0, ncols_total, lane, vec, sm);
+        __syncwarp();
+        const int j = j0 + lane;
+        if (j < n_tiles) {
+            float v[kVocabTile];
+            read_tile<kDtype>(sm, lane, v);
+            const int ncols = min(kVocabTile, V - j * kVocabTile);
+            if (targets) {
+                const int64_t tl = static_cast<int64_t>(targets[t]) - static_cast<int64_t>(j) * kVocabTile;
+                if (tl >= 0 && tl < ncols) {
+                    float tv = 0.0f;
+#pragma unroll
+                    for (int c = 0; c < kVocabTile; ++c) tv = (c == tl) ? v[c] : tv;
+                    tgt_logit[t] = tv;
+                }
             }
+            // columns past the vocabulary are not part of the tile: -inf, whose
+            // exp is +0, so their tree partners pass through unchanged
+            if (ncols < kVocabTile) {
+#pragma unroll
+                for (int c = 0; c < kVocabTile; ++c)
+                    if (c >= ncols) v[c] = -CUDART_INF_F;
+            }
+            float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+#pragma unroll
+            for (int c = 4; c < kVocabTile; c += 4) {
+                m0 = fmaxf(m0, v[c]);
+                m1 = fmaxf(m1, v[c + 1]);
+                m2 = fmaxf(m2, v[c + 2]);
+                m3 = fmaxf(m3, v[c + 3]);
+            }
+            const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+#pragma unroll
+            for (int c = 0; c < kVocabTile; ++c) v[c] = contract_exp(__fsub_rn(v[c], m));
+#pragma unroll
+            for (int w = kVocabTile / 2; w >= 1; w >>= 1) {
+#pragma unroll
+                for (int i = 0; i < w; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
+            }
+            partials[static_cast<int64_t>(t) * n_tiles + j] = make_float2(m, v[0]);
         }
     }
 }
@@ -156,12 +229,24 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// fp32 slices are the larger: 4 warps x 32 tiles x 132 x 4 B = 66 KB, 3 CTAs per SM
+constexpr int kMatSmem = kMatWarps * kSliceTiles * Pitch<RLK_DTYPE_F32>::value * 4;
+
+// Every row starts on a 16-byte boundary (16-byte copies of whole chunks).
 bool rows_vector_aligned(const void* logits, int dtype, int64_t ld) {
-    const uintptr_t a = dtype == RLK_DTYPE_F32 ? 16 : 8;
-    return (reinterpret_cast<uintptr_t>(logits) % a) == 0 && ld % 4 == 0;
+    const int64_t row_bytes = ld * (dtype == RLK_DTYPE_F32 ? 4 : 2);
+    return (reinterpret_cast<uintptr_t>(logits) % 16) == 0 && row_bytes % 16 == 0;
 }
 
 }  // namespace
+
+cudaError_t prepare_mat_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_F32>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_BF16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+}
 
 cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
                                      const int32_t* targets, const uint8_t* active, int T, int V,
@@ -169,16 +254,18 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
                                      cudaStream_t stream) {
     const int n_tiles = (V + kVocabTile - 1) / kVocabTile;
     const bool vec = rows_vector_aligned(logits, dtype, ld);
-    const int64_t runs = static_cast<int64_t>(T) * ((n_tiles + 15) / 16);
-    int64_t blocks = (runs + kMatWarps - 1) / kMatWarps;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    const int64_t tasks = static_cast<int64_t>(T) * ((n_tiles + kSliceTiles - 1) / kSliceTiles);
+    int64_t blocks = (tasks + kMatWarps - 1) / kMatWarps;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (dtype == RLK_DTYPE_F32)
-        k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32, 0, stream>>>(
-            logits, ld, vec, targets, active, T, V, n_tiles, partials, tgt_logit);
+        k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32, kMatSmem,
+                                             stream>>>(logits, ld, vec, targets, active, T, V,
+                                                       n_tiles, partials, tgt_logit);
     else
-        k_mat_tile_partials<RLK_DTYPE_BF16><<<static_cast<int>(blocks), kMatWarps * 32, 0, stream>>>(
-            logits, ld, vec, targets, active, T, V, n_tiles, partials, tgt_logit);
+        k_mat_tile_partials<RLK_DTYPE_BF16><<<static_cast<int>(blocks), kMatWarps * 32, kMatSmem,
+                                              stream>>>(logits, ld, vec, targets, active, T, V,
+                                                        n_tiles, partials, tgt_logit);
     return cudaGetLastError();
 }
 
