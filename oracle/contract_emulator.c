@@ -313,6 +313,66 @@ void emu_grad_logits(const float* logits, int64_t T, int64_t V, const float* lse
     }
 }
 
+/*
+ * Strict RMSNorm ("RMSNorm" row of the strict-path table: reduction domain,
+ * epsilon, residual add, output boundary), as this library reads it:
+ *   x'   = bf16_RN(RN(x + r))                     (residual add, if given)
+ *   s    = pairwise tree over nextpow2(H) feature slots of RN(x'_i * x'_i)
+ *          (exact products; slots >= H absent)
+ *   a    = RN(RN(s / H) + eps)
+ *   rstd = rlk_rsqrt(a)
+ *   y_i  = bf16_RN(RN(RN(x'_i * rstd) * gamma_i))
+ * rlk_rsqrt: seed 0x5f375a86 - (bits(a) >> 1) (Lomont's constant for the
+ * classic bit-level inverse-square-root estimate), two Newton steps
+ * y <- RN(y * fma(-RN(a/2), RN(y*y), 1.5)), then one in correction form
+ * y <- fma(y, fma(-RN(a/2), RN(y*y), 0.5), y).
+ */
+float emu_rsqrt(float a) {
+    uint32_t i = 0x5f375a86u - (f2u(a) >> 1);
+    float y = u2f(i);
+    float h = 0.5f * a;
+    for (int k = 0; k < 2; ++k) {
+        float r = y * y;
+        float t = fmaf(-h, r, 1.5f);
+        y = y * t;
+    }
+    /* last step in correction form: y + y * (0.5 - h y^2), one rounding for the update */
+    float e = fmaf(-h, y * y, 0.5f);
+    return fmaf(y, e, y);
+}
+
+static float bf16_to_f32(uint16_t b) { return u2f((uint32_t)b << 16); }
+
+void emu_rmsnorm(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps,
+                 int64_t T, int64_t H, uint16_t* y, uint16_t* xr_out) {
+    int64_t slots = 1;
+    while (slots < H) slots *= 2;
+    float* q = (float*)malloc(sizeof(float) * (size_t)slots);
+    float* xr = (float*)malloc(sizeof(float) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < H; ++i) {
+            float v = bf16_to_f32(x[t * H + i]);
+            if (res) {
+                uint16_t b = bf16_rne(v + bf16_to_f32(res[t * H + i]));
+                if (xr_out) xr_out[t * H + i] = b;
+                v = bf16_to_f32(b);
+            }
+            xr[i] = v;
+        }
+        for (int64_t i = 0; i < slots; ++i) q[i] = i < H ? xr[i] * xr[i] : 0.0f;
+        for (int64_t w = slots; w > 1; w /= 2)
+            for (int64_t i = 0; i < w / 2; ++i) q[i] = q[2 * i] + q[2 * i + 1];
+        float mean = q[0] / (float)H;
+        float rstd = emu_rsqrt(mean + eps);
+        for (int64_t i = 0; i < H; ++i)
+            y[t * H + i] = bf16_rne((xr[i] * rstd) * bf16_to_f32(gamma[i]));
+    }
+    free(q);
+    free(xr);
+}
+
+void emu_rsqrt_sweep(float lo, float hi, double* max_ulp, float* worst_x, int64_t* count);
+
 /* ---- exhaustive accuracy sweeps against fp64 libm (the independent reference) ---- */
 static double ulp_err(float y, double z) {
     if (z == 0.0) return y == 0.0f ? 0.0 : INFINITY;
@@ -395,4 +455,34 @@ void emu_constants(float* out /* 16 */) {
     out[0] = c_log2e; out[1] = c_ln2_hi; out[2] = c_ln2_lo; out[3] = c_shifter; out[4] = c_sqrt2;
     for (int k = 0; k < 8; ++k) out[5 + k] = c_taylor[k];
     out[13] = c_atanh[0]; out[14] = c_atanh[1]; out[15] = c_atanh[4];
+}
+
+void emu_rsqrt_sweep(float lo, float hi, double* max_ulp, float* worst_x, int64_t* count) {
+    uint32_t a = f2u(lo), b = f2u(hi);
+    double best = 0.0;
+    float wx = 0.0f;
+    int64_t cnt = 0;
+    #pragma omp parallel
+    {
+        double lbest = 0.0;
+        float lwx = 0.0f;
+        int64_t lcnt = 0;
+        #pragma omp for schedule(static)
+        for (int64_t u = (int64_t)a; u <= (int64_t)b; ++u) {
+            float x = u2f((uint32_t)u);
+            float y = emu_rsqrt(x);
+            double z = 1.0 / sqrt((double)x);
+            double err = ulp_err(y, z);
+            if (err > lbest) { lbest = err; lwx = x; }
+            ++lcnt;
+        }
+        #pragma omp critical
+        {
+            if (lbest > best) { best = lbest; wx = lwx; }
+            cnt += lcnt;
+        }
+    }
+    *max_ulp = best;
+    *worst_x = wx;
+    *count = cnt;
 }

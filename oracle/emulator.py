@@ -48,6 +48,12 @@ def lib():
         L.emu_log_softmax.argtypes = [P, i64, i64, P, P, P]
         L.emu_grad_logits.restype = None
         L.emu_grad_logits.argtypes = [P, i64, i64, P, P, P, P, P]
+        L.emu_rsqrt.restype = f
+        L.emu_rsqrt.argtypes = [f]
+        L.emu_rsqrt_sweep.restype = None
+        L.emu_rsqrt_sweep.argtypes = [f, f, P, P, P]
+        L.emu_rmsnorm.restype = None
+        L.emu_rmsnorm.argtypes = [P, P, P, f, i64, i64, P, P]
         L.emu_constants.restype = None
         L.emu_constants.argtypes = [P]
         _lib = L
@@ -189,3 +195,26 @@ def exact_fp32_logits(logits_f64: np.ndarray) -> np.ndarray:
         raise ValueError("logits are not exactly representable in fp32")
     return L32
 
+
+
+def rsqrt(x: float) -> np.float32:
+    return np.float32(lib().emu_rsqrt(ctypes.c_float(x)))
+
+
+def rsqrt_sweep(lo: float, hi: float):
+    mu, wx, cnt = ctypes.c_double(), ctypes.c_float(), ctypes.c_int64()
+    lib().emu_rsqrt_sweep(lo, hi, ctypes.byref(mu), ctypes.byref(wx), ctypes.byref(cnt))
+    return mu.value, wx.value, cnt.value
+
+
+def rmsnorm(x_bits: np.ndarray, gamma_bits: np.ndarray, eps: float,
+            residual_bits: Optional[np.ndarray] = None):
+    """Contract RMSNorm -> (y bf16 bits [T, H], x' bf16 bits [T, H] or None)."""
+    x = np.ascontiguousarray(x_bits, np.uint16)
+    T, H = x.shape
+    g = np.ascontiguousarray(gamma_bits, np.uint16)
+    r = None if residual_bits is None else np.ascontiguousarray(residual_bits, np.uint16)
+    y = np.empty((T, H), np.uint16)
+    xr = None if r is None else np.empty((T, H), np.uint16)
+    lib().emu_rmsnorm(_ptr(x), _ptr(r), _ptr(g), ctypes.c_float(eps), T, H, _ptr(y), _ptr(xr))
+    return y, xr
