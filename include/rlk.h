@@ -276,6 +276,27 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
                                          int32_t* dev_status, rlk_stream_t stream);
 
 /*
+ * Strict RMSNorm producing the hidden states the head consumes (the
+ * strict-path table's "RMSNorm" row: reduction domain, epsilon, residual
+ * add, output boundary).  Per row:
+ *   x'   = bf16_RN(RN(x + residual))          (x itself when residual is NULL)
+ *   s    = pairwise tree over nextpow2(H) feature slots of x'_i^2 (fp32)
+ *   rstd = rlk_rsqrt(RN(RN(s / H) + eps))      (the library's own rsqrt)
+ *   out  = bf16_RN(RN(RN(x'_i * rstd) * gamma_i))
+ * A row's result does not depend on the batch around it.
+ *
+ *   x, residual  device, bf16 [T][H] (residual may be NULL), 16-byte aligned
+ *   gamma        device, bf16 [H]
+ *   eps          > 0
+ *   out          device, bf16 [T][H]
+ *   residual_out device, bf16 [T][H] receiving x' (the next residual stream), or NULL;
+ *                requires residual
+ *   H            multiple of 64, at most 8192
+ */
+rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma, float eps,
+                         int64_t T, int64_t H, void* out, void* residual_out, rlk_stream_t stream);
+
+/*
  * Same result as rlk_linear_logprob (same kernels, same bits), for callers
  * that cannot allocate device memory when they call: e.g. a rollout engine
  * that reserved almost all GPU memory for its KV cache at start-up, or a

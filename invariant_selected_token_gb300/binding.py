@@ -29,7 +29,7 @@ EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rl
             "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
             "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
             "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax",
-            "rlk_backward_workspace_size", "rlk_linear_logprob_backward"]
+            "rlk_backward_workspace_size", "rlk_linear_logprob_backward", "rlk_rmsnorm"]
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_linear_logprob_backward.restype = i32
         L.rlk_linear_logprob_backward.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, P, sz, P,
                                                   P]
+        L.rlk_rmsnorm.restype = i32
+        L.rlk_rmsnorm.argtypes = [P, P, P, ctypes.c_float, i64, i64, P, P, P]
         L.rlk_log_softmax.restype = i32
         L.rlk_log_softmax.argtypes = [P, i32, i64, P, i64, i64, P, P, P, sz, P, P]
         _lib = L
@@ -351,3 +353,23 @@ def linear_logprob_backward(hidden, W, targets, grad_logprob, lse, active=None,
         _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
         "rlk_linear_logprob_backward")
     return (grad_hidden if want_hidden else None), (grad_W if want_W else None)
+
+
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
+            residual: Optional[torch.Tensor] = None, want_residual_out: bool = False,
+            out=None, residual_out=None, stream=None):
+    """Strict RMSNorm -> (out bf16 [T, H], residual_out bf16 [T, H] or None)."""
+    dev = x.device
+    _require(x, torch.bfloat16, "x", ndim=2)
+    _require(gamma, torch.bfloat16, "gamma", dev, ndim=1)
+    if residual is not None:
+        _require(residual, torch.bfloat16, "residual", dev, ndim=2)
+    T, H = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    if want_residual_out and residual_out is None:
+        residual_out = torch.empty_like(x)
+    _check(lib().rlk_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
+                             _ptr(residual_out if want_residual_out else None),
+                             _stream(dev, stream)), "rlk_rmsnorm")
+    return out, (residual_out if want_residual_out else None)

@@ -668,4 +668,33 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
     return RLK_OK;
 }
 
+rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma, float eps,
+                         int64_t T, int64_t H, void* out, void* residual_out,
+                         rlk_stream_t stream) {
+    if (T < 0 || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (H < 64 || H % 64 != 0 || H > 8192) return RLK_ERR_UNSUPPORTED;
+    if (!(eps > 0.0f) || !(eps < 3.0e38f)) return RLK_ERR_INVALID_ARG;
+    if (T == 0) return RLK_OK;
+    if (!x || !gamma || !out || (residual_out && !residual)) return RLK_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(gamma, 16) || !aligned(out, 16) ||
+        !aligned(residual_out, 16))
+        return RLK_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    rlk_status_t s = device_check(&dev);
+    if (s != RLK_OK) return s;
+    rlk::RmsNormArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.res = static_cast<const uint16_t*>(residual);
+    a.gamma = static_cast<const uint16_t*>(gamma);
+    a.eps = eps;
+    a.T = int(T);
+    a.H = int(H);
+    a.y = static_cast<uint16_t*>(out);
+    a.res_out = static_cast<uint16_t*>(residual_out);
+    return rlk::launch_rmsnorm(a, dev->sm_count, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -105,6 +105,18 @@ cudaError_t prepare_gemm_kernels();
 cudaError_t launch_sum_splits(const float* parts, int64_t split_stride, int splits, int64_t n,
                               float* out, int num_sms, cudaStream_t stream);
 
+struct RmsNormArgs {
+    const uint16_t* x;        // bf16 [T][H]
+    const uint16_t* res;      // bf16 [T][H] or nullptr
+    const uint16_t* gamma;    // bf16 [H]
+    float eps;
+    int T, H;
+    uint16_t* y;              // bf16 [T][H]
+    uint16_t* res_out;        // bf16 [T][H] (x + res) or nullptr
+};
+
+cudaError_t launch_rmsnorm(const RmsNormArgs& a, int num_sms, cudaStream_t stream);
+
 struct ShardMergeArgs {
     const rlk_partial_t* parts[RLK_MAX_SHARDS];
     int n_shards;

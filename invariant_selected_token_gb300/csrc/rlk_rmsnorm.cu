@@ -1,0 +1,149 @@
+// Strict RMSNorm producing the head's hidden states ("vLLM RL-Kernel v0.1.0:
+// ROCm 上でのビット単位のトレーニング-ロールアウト一貫性", strict-path table, row
+// "RMSNorm": reduction domain, epsilon, residual add, output boundary).
+//
+// Contract, per row:
+//   x'   = bf16_RN(RN(x + r))                       residual add (optional)
+//   s    = pairwise tree over nextpow2(H) feature slots of RN(x'_i * x'_i)
+//          (products of bf16 values are exact in fp32; slots >= H absent)
+//   a    = RN(RN(s / H) + eps)
+//   rstd = rlk_rsqrt(a)
+//   y_i  = bf16_RN(RN(RN(x'_i * rstd) * gamma_i))
+//
+// One warp per row.  Element i = 256 k + 8 l + j is lane l's j-th value of
+// column group k, so each lane reads 16 contiguous bytes per group (the warp
+// reads 512 contiguous bytes) and the tree's levels fall as: 1-3 over j
+// inside the lane, 4-8 over l across lanes (xor 1..16, lower lane on the
+// left), the rest over k inside the lane -- the contract's pairwise tree
+// over the feature index, whatever the row's position in the batch.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "rlk_internal.h"
+
+namespace rlk {
+namespace {
+
+// rsqrt(a) for positive normal a: Lomont's seed for the bit-level inverse
+// square-root estimate, two Newton steps, then one in correction form.
+// Under 0.86 ulp over [2^-40, 2^40] (checked exhaustively on the CPU).
+__device__ __forceinline__ float contract_rsqrt(float a) {
+    float y = __uint_as_float(0x5f375a86u - (__float_as_uint(a) >> 1));
+    const float h = __fmul_rn(0.5f, a);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) y = __fmul_rn(y, __fmaf_rn(-h, __fmul_rn(y, y), 1.5f));
+    const float e = __fmaf_rn(-h, __fmul_rn(y, y), 0.5f);
+    return __fmaf_rn(y, e, y);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// kK column groups of 256 features per row (nextpow2(H) / 256, at least 1).
+template <int kK>
+__global__ void __launch_bounds__(256)
+    k_rmsnorm(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
+              int H, uint16_t* y, uint16_t* res_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+         t < T; t += warps) {
+        const uint16_t* xr = x + t * H;
+        uint4 v[kK];  // x' of this lane, 8 bf16 per group
+        float part[kK];
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const int i0 = 256 * k + 8 * lane;
+            if (i0 < H) {
+                uint4 q = *reinterpret_cast<const uint4*>(xr + i0);
+                if (res) {
+                    const uint4 r = *reinterpret_cast<const uint4*>(res + t * H + i0);
+                    q.x = pack_bf16(__fadd_rn(bf16_lo(q.x), bf16_lo(r.x)), __fadd_rn(bf16_hi(q.x), bf16_hi(r.x)));
+                    q.y = pack_bf16(__fadd_rn(bf16_lo(q.y), bf16_lo(r.y)), __fadd_rn(bf16_hi(q.y), bf16_hi(r.y)));
+                    q.z = pack_bf16(__fadd_rn(bf16_lo(q.z), bf16_lo(r.z)), __fadd_rn(bf16_hi(q.z), bf16_hi(r.z)));
+                    q.w = pack_bf16(__fadd_rn(bf16_lo(q.w), bf16_lo(r.w)), __fadd_rn(bf16_hi(q.w), bf16_hi(r.w)));
+                    if (res_out) *reinterpret_cast<uint4*>(res_out + t * H + i0) = q;
+                }
+                v[k] = q;
+                // levels 1-3: pairs (0,1),(2,3),(4,5),(6,7), then pairs of those
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                float s2[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float a = bf16_lo(w[p]), b = bf16_hi(w[p]);
+                    s2[p] = __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
+                }
+                part[k] = __fadd_rn(__fadd_rn(s2[0], s2[1]), __fadd_rn(s2[2], s2[3]));
+            } else {
+                v[k] = make_uint4(0u, 0u, 0u, 0u);
+                part[k] = 0.0f;  // absent slots: +0 passes every partner through
+            }
+        }
+        // levels 4-8 across lanes, lower lane on the left
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float other = __shfl_xor_sync(0xffffffffu, part[k], o);
+                part[k] = (lane & o) ? __fadd_rn(other, part[k]) : __fadd_rn(part[k], other);
+            }
+        }
+        // remaining levels over the column groups
+#pragma unroll
+        for (int w = kK / 2; w >= 1; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) part[i] = __fadd_rn(part[2 * i], part[2 * i + 1]);
+        }
+        const float mean = __fdiv_rn(part[0], static_cast<float>(H));
+        const float rstd = contract_rsqrt(__fadd_rn(mean, eps));
+        uint16_t* yr = y + t * H;
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const int i0 = 256 * k + 8 * lane;
+            if (i0 < H) {
+                const uint4 g = *reinterpret_cast<const uint4*>(gamma + i0);
+                const uint32_t xw[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    o[p] = pack_bf16(__fmul_rn(__fmul_rn(bf16_lo(xw[p]), rstd), bf16_lo(gw[p])),
+                                     __fmul_rn(__fmul_rn(bf16_hi(xw[p]), rstd), bf16_hi(gw[p])));
+                *reinterpret_cast<uint4*>(yr + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+template <int kK>
+cudaError_t launch_k(const RmsNormArgs& a, int num_sms, cudaStream_t stream) {
+    int64_t blocks = (static_cast<int64_t>(a.T) + 7) / 8;
+    if (blocks > static_cast<int64_t>(num_sms) * 16) blocks = static_cast<int64_t>(num_sms) * 16;
+    k_rmsnorm<kK><<<static_cast<int>(blocks), 256, 0, stream>>>(a.x, a.res, a.gamma, a.eps, a.T,
+                                                                  a.H, a.y, a.res_out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const RmsNormArgs& a, int num_sms, cudaStream_t stream) {
+    int slots = 1;
+    while (slots < a.H) slots *= 2;
+    const int k = slots <= 256 ? 1 : slots / 256;
+    switch (k) {
+        case 1: return launch_k<1>(a, num_sms, stream);
+        case 2: return launch_k<2>(a, num_sms, stream);
+        case 4: return launch_k<4>(a, num_sms, stream);
+        case 8: return launch_k<8>(a, num_sms, stream);
+        case 16: return launch_k<16>(a, num_sms, stream);
+        case 32: return launch_k<32>(a, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rlk

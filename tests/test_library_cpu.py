@@ -138,3 +138,15 @@ def test_materialised_logits_validation(L):
     g = L.rlk_log_softmax
     assert g(0x10000, 0, 1024, None, 4, 1000, None, 0x50000, 0x60000, 1 << 20, None, None) == 1
     assert g(0x10001, 0, 1001, None, 4, 1000, 0x40000, 0x50000, 0x60000, 1 << 20, None, None) == 3
+
+
+def test_rmsnorm_validation(L):
+    f = L.rlk_rmsnorm
+    import ctypes as C
+    ok = (0x10000, None, 0x20000, C.c_float(1e-6), 4, 4096, 0x30000, None, None)
+    assert f(*ok[:4], 4, 100, *ok[6:]) == 2           # H % 64
+    assert f(*ok[:4], 4, 16384, *ok[6:]) == 2         # H > 8192
+    assert f(0x10000, None, 0x20000, C.c_float(0.0), 4, 4096, 0x30000, None, None) == 1
+    assert f(0x10000, None, 0x20000, C.c_float(1e-6), 4, 4096, 0x30000, 0x40000, None) == 1
+    assert f(0x10008, None, 0x20000, C.c_float(1e-6), 4, 4096, 0x30000, None, None) == 3
+    assert f(0x10000, None, 0x20000, C.c_float(1e-6), 0, 4096, 0x30000, None, None) == 0
