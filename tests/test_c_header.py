@@ -1,0 +1,45 @@
+"""include/rlk.h is a plain C header: a C11 program includes it, links
+librlk.so and calls the host-only entry points (no GPU needed)."""
+import os
+import subprocess
+
+import pytest
+
+from invariant_selected_token_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "rlk.h"
+
+int main(void) {
+    int64_t b = 0, e = 0;
+    if (strcmp(rlk_contract_id(), "rlk-linlogp-v1") != 0) return 1;
+    if (rlk_shard_range(151936, 4, 3, &b, &e) != RLK_OK) return 2;
+    if (b != 891 * RLK_VOCAB_TILE || e != 151936) return 3;
+    if (rlk_workspace_size(0, 151936, 4) != 0) return 4;
+    if (rlk_linear_logprob(NULL, NULL, NULL, NULL, 4, 64, 1000, 1, NULL, NULL, NULL, 0, NULL,
+                           NULL) != RLK_ERR_INVALID_ARG) return 5;
+    if (RLK_STATIC_WS_BYTES != (16u << 20)) return 6;
+    printf("%s\n", rlk_status_string(RLK_ERR_TIMEOUT));
+    return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(tmp_path):
+    lib = build.build()
+    src = tmp_path / "use_rlk.c"
+    src.write_text(PROGRAM)
+    exe = tmp_path / "use_rlk"
+    cmd = ["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+           "-L", os.path.dirname(lib), "-lrlk", "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0 and "cannot find -lrlk" in r.stderr:
+        pytest.skip("linker cannot use librlk.so directly")
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, (out.returncode, out.stderr)
+    assert out.stdout.strip() == "RLK_ERR_TIMEOUT"
