@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any multicast
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // With programmatic dependent launch the set-up above overlaps the
+    // previous kernel; nothing it wrote or reads is touched before this point.
+    ptx::grid_dependency_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -275,6 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n_blk = unit / num_mu;
             const int m_blk = kPair ? 2 * (unit - n_blk * num_mu) + static_cast<int>(rank)
                                     : unit - n_blk * num_mu;
+            // last unit of this CTA: let the next kernel (the tile tree) start
+            // launching; it waits for this grid before reading anything
+            if (unit + ustride >= total) ptx::grid_dependents_launch();
             if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) {
                 *abort_flag = 1;
                 report(a.status, RLK_ERR_TIMEOUT);
@@ -398,8 +404,17 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     if (!pair) {
         const int64_t total = static_cast<int64_t>(num_m) * num_n;
         const int grid = static_cast<int>(total < num_sms ? total : num_sms);
-        k_tile_partials<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(map_hidden, map_w, a);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, false>, map_hidden, map_w, a);
     }
     const int64_t units = static_cast<int64_t>((num_m + 1) / 2) * num_n;
     const int clusters = static_cast<int>(units < pair_clusters ? units : pair_clusters);

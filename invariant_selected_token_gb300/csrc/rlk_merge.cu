@@ -31,6 +31,7 @@
 
 #include "rlk_contract.cuh"
 #include "rlk_internal.h"
+#include "rlk_ptx.cuh"
 
 namespace rlk {
 namespace {
@@ -170,6 +171,8 @@ __global__ void __launch_bounds__(256) k_tile_tree(const TileTreeArgs a) {
     const SlotRun run = slot_run<5>(lane, a.depth, a.n_tiles);
     // cross-lane level after which lane r << shard_level holds shard r's node
     const int shard_level = (a.depth < 5 ? a.depth : 5) - a.shard_depth;
+    ptx::grid_dependency_wait();   // the tile pairs are the previous kernel's output
+    ptx::grid_dependents_launch();
 
     for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
         const bool act = a.active ? (a.active[t] != 0) : true;
@@ -204,6 +207,8 @@ __global__ void __launch_bounds__(256) k_tile_tree_cta(const TileTreeArgs a) {
     const int warp = tid >> 5;
     const SlotRun run = slot_run<8>(tid, a.depth, a.n_tiles);
     const int shard_level = (a.depth < 8 ? a.depth : 8) - a.shard_depth;
+    ptx::grid_dependency_wait();   // the tile pairs are the previous kernel's output
+    ptx::grid_dependents_launch();
 
     for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
         const bool act = a.active ? (a.active[t] != 0) : true;
@@ -278,19 +283,35 @@ __global__ void __launch_bounds__(256) k_shard_merge(const ShardMergeArgs a) {
     }
 }
 
+// Launched with programmatic dependent launch: the grid may start while the
+// logits kernel finishes, and waits for it before reading the tile pairs.
+template <typename Kernel>
+cudaError_t launch_dependent(Kernel kernel, int blocks, const TileTreeArgs& a,
+                             cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 template <int kLogL>
 cudaError_t launch_warp_tree(const TileTreeArgs& a, cudaStream_t stream) {
     int blocks = (a.T + 7) / 8;
     if (blocks > 4096) blocks = 4096;
-    k_tile_tree<kLogL><<<blocks, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(k_tile_tree<kLogL>, blocks, a, stream);
 }
 
 template <int kLogL>
 cudaError_t launch_cta_tree(const TileTreeArgs& a, cudaStream_t stream) {
     const int blocks = a.T < 65535 ? a.T : 65535;
-    k_tile_tree_cta<kLogL><<<blocks, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(k_tile_tree_cta<kLogL>, blocks, a, stream);
 }
 
 }  // namespace

@@ -106,6 +106,20 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorM
         : "memory");
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Wait until the grids this one depends on (launched before it in the stream)
+// have completed and their memory is visible; a no-op without programmatic
+// dependent launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream to start launching (it still waits for
+// this one at its own grid_dependency_wait before touching shared data).
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
