@@ -35,6 +35,7 @@ struct DeviceState {
     int sm_count = 0;
     int cc = 0;             // 10 * major + minor
     int pair_clusters = 0;  // 2-CTA clusters of the logits kernel that fit at once
+    int mat_ctas_per_sm[2] = {0, 0};  // materialised-logits kernel, fp32 / bf16
 };
 
 std::mutex g_mutex;
@@ -121,7 +122,7 @@ rlk_status_t device_check(DeviceState** out) {
             if (rlk::prepare_tile_partials_kernels(&st.pair_clusters) != cudaSuccess)
                 return RLK_ERR_CUDA;
             if (rlk::prepare_gemm_kernels() != cudaSuccess) return RLK_ERR_CUDA;
-            if (rlk::prepare_mat_kernels() != cudaSuccess) return RLK_ERR_CUDA;
+            if (rlk::prepare_mat_kernels(st.mat_ctas_per_sm) != cudaSuccess) return RLK_ERR_CUDA;
         }
         if (!g_encode) {
             void* fn = nullptr;
@@ -525,8 +526,9 @@ rlk_status_t rlk_logits_logprob(const void* logits, int logits_dtype, int64_t ld
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (rlk::launch_mat_tile_partials(logits, logits_dtype, ld, targets, active_mask, int(T),
                                       int(V), reinterpret_cast<float2*>(ws + l.partials),
-                                      reinterpret_cast<float*>(ws + l.tgt), dev->sm_count,
-                                      st) != cudaSuccess)
+                                      reinterpret_cast<float*>(ws + l.tgt),
+                                      dev->sm_count * dev->mat_ctas_per_sm[logits_dtype], st) !=
+        cudaSuccess)
         return RLK_ERR_CUDA;
     return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse, ws, l,
                          dev_status, st);
@@ -550,8 +552,9 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (rlk::launch_mat_tile_partials(logits, logits_dtype, ld, nullptr, active_mask, int(T),
                                       int(V), reinterpret_cast<float2*>(ws + l.partials),
-                                      reinterpret_cast<float*>(ws + l.tgt), dev->sm_count,
-                                      st) != cudaSuccess)
+                                      reinterpret_cast<float*>(ws + l.tgt),
+                                      dev->sm_count * dev->mat_ctas_per_sm[logits_dtype], st) !=
+        cudaSuccess)
         return RLK_ERR_CUDA;
     if ((s = run_tile_tree(nullptr, active_mask, T, V, 1, nullptr, out_lse, ws, l, dev_status,
                            st)) != RLK_OK)

@@ -74,6 +74,64 @@ __device__ __forceinline__ float contract_log(float s) {
     return __fmaf_rn(ef, kLn2Hi, __fmaf_rn(ef, kLn2Lo, logf_));
 }
 
+// ---------------------------------------------------------------- two lanes
+// Blackwell's packed fp32 instructions (fma/add/mul .rn .f32x2) round each of
+// their two lanes exactly like the scalar instruction, so the contract's
+// arithmetic can run two values per instruction with unchanged bits.  A
+// pair's low 32 bits are its first value.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t p, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// contract_exp on both lanes, each lane bit for bit the scalar function:
+// fma(-n, c, x) is written fma(n, -c, x) (the exact product only changes
+// sign), t - shift as t + (-shift), and the scale 2^n is formed from the
+// low bits of t directly: with t = 1.5 * 2^23 + n exactly, the scalar's
+// (bits(t) - bits(1.5 * 2^23) + 127) << 23 equals bits(t) * 2^23 + bits(1.0f)
+// modulo 2^32, because bits(1.5 * 2^23) * 2^23 vanishes modulo 2^32.
+__device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
+    const uint64_t t = f2_fma(x, f2_splat(0x1.715476p+0f), f2_splat(0x1.8p+23f));
+    const uint64_t n = f2_add(t, f2_splat(-0x1.8p+23f));
+    uint64_t r = f2_fma(n, f2_splat(-0x1.62e430p-1f), x);
+    r = f2_fma(n, f2_splat(0x1.05c610p-29f), r);
+    uint64_t p = f2_fma(f2_splat(0x1.a01a02p-13f), r, f2_splat(0x1.6c16c2p-10f));
+    p = f2_fma(p, r, f2_splat(0x1.111112p-7f));
+    p = f2_fma(p, r, f2_splat(0x1.555556p-5f));
+    p = f2_fma(p, r, f2_splat(0x1.555556p-3f));
+    p = f2_fma(p, r, f2_splat(0.5f));
+    p = f2_fma(p, r, f2_splat(1.0f));
+    p = f2_fma(p, r, f2_splat(1.0f));
+    float tl, th;
+    f2_unpack(t, tl, th);
+    const uint64_t scale = f2_pack(__uint_as_float(__float_as_uint(tl) * 8388608u + 0x3F800000u),
+                                   __uint_as_float(__float_as_uint(th) * 8388608u + 0x3F800000u));
+    float yl, yh, xl, xh;
+    f2_unpack(f2_mul(p, scale), yl, yh);
+    f2_unpack(x, xl, xh);
+    return f2_pack(xl < -86.0f ? 0.0f : yl, xh < -86.0f ? 0.0f : yh);
+}
+
 // A (max, sum of exp(x - max)) pair.
 struct MaxSum {
     float m;
@@ -99,6 +157,57 @@ __device__ __forceinline__ MaxSum contract_merge(MaxSum left, MaxSum right) {
     MaxSum out;
     out.m = mh;
     out.s = (ml == -CUDART_INF_F) ? sh : scaled;
+    return out;
+}
+
+// The contract's 128-column tile reduction on values held as 64 pairs,
+// P[k] = (v[2k], v[2k+1]); padding columns must already be -inf.  Returns
+// (max, sum) with the bits of the scalar evaluation: the max is exact, each
+// exp is contract_exp of RN(v - max), and the sum is the pairwise tree over
+// the column index.  Level 1 adds the two lanes of each pair, giving s_j =
+// e_2j + e_2j+1; the level-1 sums are packed as X_j = (s_j, s_j+32), so each
+// packed add of neighbours X_2i + X_2i+1 forms the next level's nodes of
+// both 64-column halves at once, left node plus right node in each lane;
+// levels 2-6 run this way and level 7 adds the two halves.  The packed
+// levels are evaluated as a binary counter over j (a node is formed as soon
+// as both children exist), which keeps few partial sums live.
+__device__ __forceinline__ MaxSum tile_reduce_x2(uint64_t (&P)[64]) {
+    float m0, m1, m2, m3;
+    f2_unpack(P[0], m0, m1);
+    f2_unpack(P[1], m2, m3);
+#pragma unroll
+    for (int k = 2; k < 64; k += 2) {
+        float a, b, c, d;
+        f2_unpack(P[k], a, b);
+        f2_unpack(P[k + 1], c, d);
+        m0 = fmaxf(m0, a);
+        m1 = fmaxf(m1, b);
+        m2 = fmaxf(m2, c);
+        m3 = fmaxf(m3, d);
+    }
+    const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    const uint64_t neg_m = f2_splat(-m);
+    uint64_t pending[5];  // pending[L]: a finished left node of packed level L + 2
+    uint64_t x = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        float a, b, c, d;
+        f2_unpack(contract_exp_x2(f2_add(P[j], neg_m)), a, b);
+        f2_unpack(contract_exp_x2(f2_add(P[j + 32], neg_m)), c, d);
+        x = f2_pack(__fadd_rn(a, b), __fadd_rn(c, d));  // X_j
+        int level = 0;
+#pragma unroll
+        for (; level < 5; ++level) {
+            if (!(j & (1 << level))) break;
+            x = f2_add(pending[level], x);  // left sibling + this node
+        }
+        if (level < 5) pending[level] = x;
+    }
+    float z0, z1;
+    f2_unpack(x, z0, z1);  // the two 64-column halves
+    MaxSum out;
+    out.m = m;
+    out.s = __fadd_rn(z0, z1);
     return out;
 }
 

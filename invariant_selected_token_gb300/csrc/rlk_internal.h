@@ -75,11 +75,15 @@ struct TileTreeArgs {
 cudaError_t launch_tile_tree(const TileTreeArgs& a, cudaStream_t stream);
 
 // materialised logits [T][ld] (fp32 or bf16) -> the same per-tile pairs / target logits
+// resident_ctas: CTAs of the kernel (for this dtype) that fit on the device
+// at once; the grid never exceeds it (one persistent wave).
 cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
                                      const int32_t* targets, const uint8_t* active, int T, int V,
-                                     float2* partials, float* tgt_logit, int num_sms,
+                                     float2* partials, float* tgt_logit, int resident_ctas,
                                      cudaStream_t stream);
-cudaError_t prepare_mat_kernels();
+// Sets the kernels' shared-memory limits and reports the CTAs per SM of
+// k_mat_tile_partials for fp32 [0] and bf16 [1] logits.
+cudaError_t prepare_mat_kernels(int* ctas_per_sm);
 // out[t][v] = RN(l[t][v] - lse[t])
 cudaError_t launch_log_softmax_out(const void* logits, int dtype, int64_t ld, const float* lse,
                                    const uint8_t* active, int T, int V, float* out, int num_sms,

@@ -9,15 +9,19 @@
 //   k_mat_tile_partials  a warp stages 32 tiles of one row in shared memory,
 //                        then each lane reduces one whole 128-column tile in
 //                        registers with the contract's in-tile pairwise tree
-//                        (the fused epilogue's own arithmetic).  The (m, s)
-//                        pairs and the target logit go to the same workspace
-//                        layout the fused path uses, so the tile tree kernel
-//                        finishes the job unchanged.
+//                        (the fused epilogue's arithmetic, run two values per
+//                        instruction with the packed fp32 operations).  The
+//                        next slice's copies are in flight while a slice is
+//                        reduced.  The (m, s) pairs and the target logit go
+//                        to the same workspace layout the fused path uses, so
+//                        the tile tree kernel finishes the job unchanged.
 //   k_log_softmax_out    out[t, v] = RN(l[t, v] - lse[t]).
 //
 // Given the fused path's own fp32 logits, this path returns the fused path's
-// bits.  It is HBM-bound: each logit is read once (twice for log_softmax,
-// which also writes T x V floats).
+// bits.  fp32 logits are HBM-bound (each logit is read once, twice for
+// log_softmax, which also writes T x V floats); bf16 logits, half the bytes,
+// are bound by the FMA pipe: the contract's exp, the subtraction of the max
+// and the tree add are 14 FMA-pipe lane operations per logit.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -83,22 +87,29 @@ struct Pitch {
 // Copy the slice's real columns into shared memory in their input type
 // (element e of the slice at tile e/128, column e%128, tile pitch kPitch
 // elements).  Aligned rows use asynchronous 16-byte copies, all in flight
-// at once; a row tail or an unaligned row falls back to plain loads.
+// at once: lane l's i-th copy is chunk l + 32 i, and since 32 chunks span
+// whole tiles, its source advances 512 bytes and its destination a fixed
+// number of tile pitches per step.  A row tail or an unaligned row falls
+// back to plain loads.  The asynchronous copies are complete after
+// stage_wait().
 template <int kDtype>
-__device__ __forceinline__ void stage_slice(const void* row, int64_t c0, int ncols_total, int lane,
+__device__ __forceinline__ void stage_issue(const void* row, int64_t c0, int ncols_total, int lane,
                                             bool vec, void* sm_raw) {
     constexpr int kElem = kDtype == RLK_DTYPE_F32 ? 4 : 2;
     constexpr int kPitch = Pitch<kDtype>::value;
-    constexpr int kPerChunk = 16 / kElem;  // elements per 16-byte copy
+    constexpr int kPerChunk = 16 / kElem;                              // elements per copy
+    constexpr uint32_t kDstStep = (32 * kPerChunk / kVocabTile) * kPitch * kElem;
     const uint8_t* src = static_cast<const uint8_t*>(row) + c0 * kElem;
     uint8_t* sm = static_cast<uint8_t*>(sm_raw);
     const int full_chunks = vec ? ncols_total / kPerChunk : 0;
+    const int e0 = lane * kPerChunk;
+    uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(
+        sm + ((e0 / kVocabTile) * kPitch + e0 % kVocabTile) * kElem));
+    const uint8_t* from = src + e0 * kElem;
     for (int ch = lane; ch < full_chunks; ch += 32) {
-        const int e = ch * kPerChunk;
-        const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(
-            sm + ((e / kVocabTile) * kPitch + e % kVocabTile) * kElem));
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + e * kElem)
-                     : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(from) : "memory");
+        dst += kDstStep;
+        from += 512;
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     for (int e = full_chunks * kPerChunk + lane; e < ncols_total; e += 32) {
@@ -108,19 +119,24 @@ __device__ __forceinline__ void stage_slice(const void* row, int64_t c0, int nco
         else
             *reinterpret_cast<uint16_t*>(d) = reinterpret_cast<const uint16_t*>(src)[e];
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Element c of a staged tile as fp32 (bf16 widens exactly).
+__device__ __forceinline__ void stage_wait() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
+// A staged tile as 64 fp32 pairs (columns 2k, 2k+1; bf16 widens exactly).
 template <int kDtype>
-__device__ __forceinline__ void read_tile(const void* sm_raw, int tile, float (&v)[kVocabTile]) {
+__device__ __forceinline__ void read_tile_pairs(const void* sm_raw, int tile, uint64_t (&P)[64]) {
     constexpr int kPitch = Pitch<kDtype>::value;
     if (kDtype == RLK_DTYPE_F32) {
         const float* p = static_cast<const float*>(sm_raw) + tile * kPitch;
 #pragma unroll
         for (int c = 0; c < kVocabTile; c += 4) {
-            const float4 q = *reinterpret_cast<const float4*>(p + c);
-            v[c] = q.x; v[c + 1] = q.y; v[c + 2] = q.z; v[c + 3] = q.w;
+            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(p + c);
+            P[c / 2] = q.x;
+            P[c / 2 + 1] = q.y;
         }
     } else {
         const uint16_t* p = static_cast<const uint16_t*>(sm_raw) + tile * kPitch;
@@ -129,16 +145,25 @@ __device__ __forceinline__ void read_tile(const void* sm_raw, int tile, float (&
             const uint4 q = *reinterpret_cast<const uint4*>(p + c);
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[c + 2 * i] = __uint_as_float(w[i] << 16);
-                v[c + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
+            for (int i = 0; i < 4; ++i)
+                P[c / 2 + i] = f2_pack(__uint_as_float(w[i] << 16),
+                                       __uint_as_float(w[i] & 0xFFFF0000u));
         }
     }
 }
 
+// Staged element c of a tile as fp32.
 template <int kDtype>
-__global__ void __launch_bounds__(kMatWarps * 32)
+__device__ __forceinline__ float staged_value(const void* sm_raw, int tile, int c) {
+    constexpr int kPitch = Pitch<kDtype>::value;
+    if (kDtype == RLK_DTYPE_F32) return static_cast<const float*>(sm_raw)[tile * kPitch + c];
+    return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(sm_raw)[tile * kPitch + c]) << 16);
+}
+
+// Three CTAs per SM: the fp32 slices fill shared memory at three, and the
+// register cap (168) that three imply costs no spills.
+template <int kDtype>
+__global__ void __launch_bounds__(kMatWarps * 32, 3)
     k_mat_tile_partials(const void* logits, int64_t ld, bool vec, const int32_t* targets,
                         const uint8_t* active, int T, int V, int n_tiles, float2* partials,
                         float* tgt_logit) {
@@ -151,57 +176,57 @@ __global__ void __launch_bounds__(kMatWarps * 32)
     const int slices_per_row = (n_tiles + kSliceTiles - 1) / kSliceTiles;
     const int64_t n_tasks = static_cast<int64_t>(T) * slices_per_row;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kMatWarps;
-    const int elem = kDtype == RLK_DTYPE_F32 ? 4 : 2;
-    for (int64_t task = static_cast<int64_t>(blockIdx.x) * kMatWarps + warp; task < n_tasks;
-         task += stride) {
+    // the warp's tasks (row t, slice of 32 tiles), inactive rows skipped
+    auto next_active = [&](int64_t task) {
+        while (task < n_tasks && active && active[task / slices_per_row] == 0) task += stride;
+        return task;
+    };
+    auto issue = [&](int64_t task) {
         const int t = static_cast<int>(task / slices_per_row);
-        const int j0 = static_cast<int>(task - static_cast<int64_t>(t) * slices_per_row) * kSliceTiles;
-        if (active && active[t] == 0) continue;
-        const int64_t c0 = static_cast<int64_t>(j0) * kVocabTile;
+        const int64_t c0 = (task - static_cast<int64_t>(t) * slices_per_row) *
+                           static_cast<int64_t>(kSliceTiles * kVocabTile);
         const int ncols_total = min(kSliceTiles * kVocabTile, V - static_cast<int>(c0));
-        const void* row = static_cast<const uint8_t*>(logits) + static_cast<int64_t>(t) * ld * elem;
-        __syncwarp();
-        stage_slice<kDtype>(row, c0, ncols_total, lane, vec, sm);
-        __syncwarp();
-        const int j = j0 + lane;
-        if (j < n_tiles) {
-            float v[kVocabTile];
-            read_tile<kDtype>(sm, lane, v);
-            const int ncols = min(kVocabTile, V - j * kVocabTile);
+        const void* row = static_cast<const uint8_t*>(logits) + static_cast<int64_t>(t) * ld * kElem;
+        stage_issue<kDtype>(row, c0, ncols_total, lane, vec, sm);
+    };
+    int64_t task = next_active(static_cast<int64_t>(blockIdx.x) * kMatWarps + warp);
+    if (task < n_tasks) issue(task);
+    // Software pipeline: the slice is copied into registers (one tile per
+    // lane), the next slice's copies are issued into the freed buffer, and
+    // the reduction runs while they are in flight.
+    while (task < n_tasks) {
+        stage_wait();
+        const int t = static_cast<int>(task / slices_per_row);
+        const int j = static_cast<int>(task - static_cast<int64_t>(t) * slices_per_row) * kSliceTiles + lane;
+        const bool own = j < n_tiles;
+        const int ncols = own ? min(kVocabTile, V - j * kVocabTile) : 0;
+        uint64_t P[64];
+        if (own) {
             if (targets) {
                 const int64_t tl = static_cast<int64_t>(targets[t]) - static_cast<int64_t>(j) * kVocabTile;
-                if (tl >= 0 && tl < ncols) {
-                    float tv = 0.0f;
-#pragma unroll
-                    for (int c = 0; c < kVocabTile; ++c) tv = (c == tl) ? v[c] : tv;
-                    tgt_logit[t] = tv;
-                }
+                if (tl >= 0 && tl < ncols) tgt_logit[t] = staged_value<kDtype>(sm, lane, static_cast<int>(tl));
             }
+            read_tile_pairs<kDtype>(sm, lane, P);
+        }
+        __syncwarp();  // every lane has its tile: the buffer is free
+        const int64_t next = next_active(task + stride);
+        if (next < n_tasks) issue(next);
+        if (own) {
             // columns past the vocabulary are not part of the tile: -inf, whose
             // exp is +0, so their tree partners pass through unchanged
             if (ncols < kVocabTile) {
 #pragma unroll
-                for (int c = 0; c < kVocabTile; ++c)
-                    if (c >= ncols) v[c] = -CUDART_INF_F;
+                for (int k = 0; k < 64; ++k) {
+                    float a, b;
+                    f2_unpack(P[k], a, b);
+                    P[k] = f2_pack(2 * k < ncols ? a : -CUDART_INF_F,
+                                   2 * k + 1 < ncols ? b : -CUDART_INF_F);
+                }
             }
-            float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
-#pragma unroll
-            for (int c = 4; c < kVocabTile; c += 4) {
-                m0 = fmaxf(m0, v[c]);
-                m1 = fmaxf(m1, v[c + 1]);
-                m2 = fmaxf(m2, v[c + 2]);
-                m3 = fmaxf(m3, v[c + 3]);
-            }
-            const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-#pragma unroll
-            for (int c = 0; c < kVocabTile; ++c) v[c] = contract_exp(__fsub_rn(v[c], m));
-#pragma unroll
-            for (int w = kVocabTile / 2; w >= 1; w >>= 1) {
-#pragma unroll
-                for (int i = 0; i < w; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
-            }
-            partials[static_cast<int64_t>(t) * n_tiles + j] = make_float2(m, v[0]);
+            const MaxSum r = tile_reduce_x2(P);
+            partials[static_cast<int64_t>(t) * n_tiles + j] = make_float2(r.m, r.s);
         }
+        task = next;
     }
 }
 
@@ -240,24 +265,31 @@ bool rows_vector_aligned(const void* logits, int dtype, int64_t ld) {
 
 }  // namespace
 
-cudaError_t prepare_mat_kernels() {
+cudaError_t prepare_mat_kernels(int* ctas_per_sm) {
     cudaError_t e = cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_F32>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_BF16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_BF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &ctas_per_sm[0], k_mat_tile_partials<RLK_DTYPE_F32>, kMatWarps * 32, kMatSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &ctas_per_sm[1], k_mat_tile_partials<RLK_DTYPE_BF16>, kMatWarps * 32, kMatSmem);
+    if (e == cudaSuccess && (ctas_per_sm[0] < 1 || ctas_per_sm[1] < 1)) e = cudaErrorInvalidConfiguration;
+    return e;
 }
 
 cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
                                      const int32_t* targets, const uint8_t* active, int T, int V,
-                                     float2* partials, float* tgt_logit, int num_sms,
+                                     float2* partials, float* tgt_logit, int resident_ctas,
                                      cudaStream_t stream) {
     const int n_tiles = (V + kVocabTile - 1) / kVocabTile;
     const bool vec = rows_vector_aligned(logits, dtype, ld);
     const int64_t tasks = static_cast<int64_t>(T) * ((n_tiles + kSliceTiles - 1) / kSliceTiles);
     int64_t blocks = (tasks + kMatWarps - 1) / kMatWarps;
-    const int64_t cap = static_cast<int64_t>(num_sms) * 8;
-    if (blocks > cap) blocks = cap;
+    if (blocks > resident_ctas) blocks = resident_ctas;
     if (dtype == RLK_DTYPE_F32)
         k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32, kMatSmem,
                                              stream>>>(logits, ld, vec, targets, active, T, V,
