@@ -123,6 +123,7 @@ rlk_status_t device_check(DeviceState** out) {
                 return RLK_ERR_CUDA;
             if (rlk::prepare_gemm_kernels() != cudaSuccess) return RLK_ERR_CUDA;
             if (rlk::prepare_mat_kernels(st.mat_ctas_per_sm) != cudaSuccess) return RLK_ERR_CUDA;
+            if (rlk::prepare_tree_kernels() != cudaSuccess) return RLK_ERR_CUDA;
         }
         if (!g_encode) {
             void* fn = nullptr;
@@ -273,7 +274,8 @@ rlk_status_t common_checks(const void* hidden, const void* W, const int32_t* tar
 // shard records, then lse (and logprob when targets is not null).
 rlk_status_t run_tile_tree(const int32_t* targets, const uint8_t* active, int64_t T, int64_t V,
                            int n_shards, float* out_logprob, float* out_lse, uint8_t* ws,
-                           const Layout& l, int32_t* status, cudaStream_t stream) {
+                           const Layout& l, int32_t* status, cudaStream_t stream,
+                           const DeviceState* dev) {
     const int64_t nt = n_tiles_of(V);
     rlk::TileTreeArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -302,7 +304,7 @@ rlk_status_t run_tile_tree(const int32_t* targets, const uint8_t* active, int64_
     a.out_logprob = out_logprob;
     a.out_lse = out_lse;
     a.records = reinterpret_cast<rlk_partial_t*>(ws + l.records);
-    return rlk::launch_tile_tree(a, stream) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+    return rlk::launch_tile_tree(a, dev->sm_count, stream) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 
 // Checks shared by the two materialised-logits calls.
@@ -400,7 +402,7 @@ rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, 
     if ((s = device_check(&dev)) != RLK_OK) return s;
     return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse,
                          static_cast<uint8_t*>(workspace), l, dev_status,
-                         reinterpret_cast<cudaStream_t>(stream));
+                         reinterpret_cast<cudaStream_t>(stream), dev);
 }
 
 rlk_status_t rlk_linear_logprob(const void* hidden, const void* W, const int32_t* targets,
@@ -459,7 +461,7 @@ rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
     a.own_end = ve;
     a.V_total = V_total;
     a.records = out_partial;
-    return rlk::launch_tile_tree(a, st) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+    return rlk::launch_tile_tree(a, dev->sm_count, st) == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 
 rlk_status_t rlk_lse_merge(const rlk_partial_t* const* partials, int n_shards, int64_t T,
@@ -531,7 +533,7 @@ rlk_status_t rlk_logits_logprob(const void* logits, int logits_dtype, int64_t ld
         cudaSuccess)
         return RLK_ERR_CUDA;
     return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse, ws, l,
-                         dev_status, st);
+                         dev_status, st, dev);
 }
 
 rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
@@ -557,7 +559,7 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
         cudaSuccess)
         return RLK_ERR_CUDA;
     if ((s = run_tile_tree(nullptr, active_mask, T, V, 1, nullptr, out_lse, ws, l, dev_status,
-                           st)) != RLK_OK)
+                           st, dev)) != RLK_OK)
         return s;
     return rlk::launch_log_softmax_out(logits, logits_dtype, ld, out_lse, active_mask, int(T),
                                        int(V), out, dev->sm_count, st) == cudaSuccess

@@ -72,7 +72,9 @@ struct TileTreeArgs {
     rlk_partial_t* records;   // full: [n_shards][T]; shard: [T]
 };
 
-cudaError_t launch_tile_tree(const TileTreeArgs& a, cudaStream_t stream);
+cudaError_t launch_tile_tree(const TileTreeArgs& a, int num_sms, cudaStream_t stream);
+// Sets the warp-per-token tree kernels' shared-memory limit (staged rows).
+cudaError_t prepare_tree_kernels();
 
 // materialised logits [T][ld] (fp32 or bf16) -> the same per-tile pairs / target logits
 // resident_ctas: CTAs of the kernel (for this dtype) that fit on the device
