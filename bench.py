@@ -45,10 +45,12 @@ def parse():
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode256",
-                            "logits_fp32", "logits_bf16", "backward"],
+                            "logits_fp32", "logits_bf16", "backward", "grpo"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
-                        "materialised in HBM, reduced by the materialised-logits path")
+                        "materialised in HBM, reduced by the materialised-logits path; "
+                        "backward: the deterministic backward of the packed batch; grpo: the "
+                        "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -133,19 +135,23 @@ class ClockSampler:
 
 def k1_traffic_record(workload):
     """Per-launch DRAM bytes of the tile-partials kernel from the committed ncu summary of
-    this workload, if it was taken from the library build that is loaded now (else None)."""
+    this workload, if the loaded library was built from the sources here and the kernel's
+    translation unit is the one the counters were taken from (else None)."""
     path = os.path.join(ROOT, "profiles", "tile_partials_%s.md" % workload)
     try:
+        import re
         from invariant_selected_token_gb300 import binding
-        digest = binding.build_fingerprint().split("rev=")[1].split(";")[0]
+        from invariant_selected_token_gb300 import build as lib_build
+        loaded = binding.build_fingerprint().split("rev=")[1].split(";")[0]
+        if loaded != "src-" + lib_build.source_digest():
+            return None
         rec = {}
         with open(path) as f:
             for line in f:
                 if ":" in line and line.strip().startswith("- "):
                     k, v = line.strip()[2:].split(":", 1)
                     rec[k.strip()] = v.strip().strip("`")
-        if rec.get("library_rev", "").split()[0].strip("`") == digest:
-            import re
+        if rec.get("kernel_unit_rev", "").split()[0].strip("`") == lib_build.unit_digest("rlk_logits.cu"):
             return int(re.search(r"\d+", rec["dram_bytes_per_launch"]).group(0))
     except Exception:
         pass
@@ -319,6 +325,135 @@ def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
     return 0
 
 
+def grpo_arm(args, rank, world, dev, dist, W, binding, WL):
+    """The long-response GRPO batch: 8 prompts x 8 samples, prompt rows inactive, response
+    rows active, packed back to back and processed in 8192-row calls.  One step = every
+    call of the batch; tokens counted are the active (response) rows."""
+    import torch
+    g = WL.grpo_long(W, dev, seed=1235 + 1000 * rank)
+    chunks = g.meta["chunks"]
+    N = g.hidden.shape[0]
+    n_active = int(g.active.sum().item())
+    rows_max = max(r1 - r0 for r0, r1 in chunks)
+    ws = binding.new_workspace(rows_max, V, N_SHARDS, dev)
+    out_lp = torch.empty(N, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(N, dtype=torch.float32, device=dev)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k1_events=None):
+        for i, (r0, r1) in enumerate(chunks):
+            if k1_events is not None:
+                k1_events[i][0].record(stream)
+            binding.tile_partials(g.hidden[r0:r1], W, g.targets[r0:r1], g.active[r0:r1],
+                                  N_SHARDS, ws, status, stream)
+            if k1_events is not None:
+                k1_events[i][1].record(stream)
+            binding.tile_merge(g.targets[r0:r1], g.active[r0:r1], V, N_SHARDS, out_lp[r0:r1],
+                               out_lse[r0:r1], ws, status, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status)
+    K = args.steps
+    k1_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in chunks] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        step(k1_ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(t0, time.time())
+    binding.raise_on_device_status(status)
+    ms_total = max_over_ranks(start.elapsed_time(end), dist, dev)
+    k1_ms_step = statistics.mean(sum(a.elapsed_time(b) for a, b in ev) for ev in k1_ev)
+
+    e2e = None
+    if not args.no_e2e:
+        h_hidden = g.hidden.cpu().pin_memory()
+        h_tg = g.targets.cpu().pin_memory()
+        h_act = g.active.cpu().pin_memory()
+        h_lp = torch.empty(N, dtype=torch.float32).pin_memory()
+        h_lse = torch.empty(N, dtype=torch.float32).pin_memory()
+        d_hidden = torch.empty_like(g.hidden)
+        d_tg = torch.empty_like(g.targets)
+        d_act = torch.empty_like(g.active)
+
+        def e2e_step():
+            d_hidden.copy_(h_hidden, non_blocking=True)
+            d_tg.copy_(h_tg, non_blocking=True)
+            d_act.copy_(h_act, non_blocking=True)
+            for r0, r1 in chunks:
+                binding.linear_logprob(d_hidden[r0:r1], W, d_tg[r0:r1], d_act[r0:r1], N_SHARDS,
+                                       out_lp[r0:r1], out_lse[r0:r1], ws, status, stream)
+            h_lp.copy_(out_lp, non_blocking=True)
+            h_lse.copy_(out_lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e = {"value": weak_scaling_value(world, n_active, K, e_ms), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(N * (H * 2 + 4 + 1)),
+               "d2h_bytes_per_step": int(N * 8)}
+
+    peaks = load_peaks()
+    flops = 2.0 * N * H * V  # every row of every call goes through the GEMM
+    achieved = flops / (k1_ms_step / 1000.0) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": None, "peak_kind": "burst bf16 (%s)" % peaks["source"],
+                "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+                "kernel": "k_tile_partials", "kernel_ms_per_step": round(k1_ms_step, 4),
+                "launches_per_step": len(chunks),
+                "algorithmic": {"flops_per_step": flops, "rows_per_step": N,
+                                "active_rows_per_step": n_active}}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        act_rows = torch.nonzero(g.active).flatten().cpu().numpy()
+        rows = act_rows[WL.permutation(len(act_rows), 4321)[:24]]
+        W_bits = WL.bf16_tensor_bits(W)
+        hid_bits = WL.bf16_tensor_bits(g.hidden[torch.from_numpy(rows).to(dev)])
+        s_, n_ = cpu_oracle_sample(hid_bits, W_bits, g.targets.cpu().numpy()[rows], None)
+        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "%d active rows of the batch over the full vocabulary (%.1f s)" % (n_, s_)}
+    if rank == 0:
+        ms_per_step = ms_total / K
+        out = {"metric": METRIC, "value": weak_scaling_value(world, n_active, K, ms_total),
+               "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
+               "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "long-response GRPO batch: 8 prompts x 8 samples, prompt "
+                                      "U[64,512] rows inactive, response U[256,6912] rows active, "
+                                      "%d rows (%d active) in %d calls of <= 8192 rows, H=4096, "
+                                      "V=151936, bf16, 4 vocab shards" % (N, n_active, len(chunks)),
+                          "rows": N, "active_rows": n_active, "calls_per_step": len(chunks),
+                          "tokens_counted": "active rows", "H": H, "V": V, "n_shards": N_SHARDS,
+                          "l2": "inputs larger than L2 (W = 1.24 GB, hidden %.2f GB)"
+                                % (N * H * 2 / 1e9),
+                          "parallelism": "dp%d (independent batches)" % world},
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+               "gpu_launches": 2 * len(chunks) * K, "clocks": clk,
+               "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out))
+    return 0
+
+
 def backward_arm(args, rank, world, dev, dist, W, pk, binding):
     """grad_hidden and grad_W of sum_t g[t] logprob[t] for the packed batch."""
     import torch
@@ -406,6 +541,8 @@ def main():
     binding.lib()
 
     W = WL.head_weights(dev)                       # same weights on every rank
+    if args.workload == "grpo":
+        return grpo_arm(args, rank, world, dev, dist, W, binding, WL)
     pk = WL.packed(W, dev, seed=rank_batch_seed(rank))  # each rank its own batch
     if args.workload.startswith("logits_"):
         return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)

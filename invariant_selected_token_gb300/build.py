@@ -61,6 +61,19 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
+def unit_digest(src: str) -> str:
+    """Digest of one translation unit's inputs: the source, every shared header, the C
+    header and the flags.  Counters taken from a kernel stay valid while it is unchanged."""
+    h = hashlib.sha256()
+    for name in [src] + HEADERS:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(INCLUDE, "rlk.h"), "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return "unit-" + h.hexdigest()[:16]
+
+
 def _compile(src: str, defines, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc()] + NVCC_FLAGS + defines + ["-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
@@ -97,4 +110,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv))
+    if "--unit-digest" in sys.argv:
+        print(unit_digest(sys.argv[sys.argv.index("--unit-digest") + 1]))
+    else:
+        print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv))

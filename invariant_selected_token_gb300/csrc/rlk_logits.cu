@@ -53,33 +53,18 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
 // pairs of those, seven levels.  A padding column is set to -inf, whose exp
 // is +0, and x + 0 = x exactly for the non-negative terms here, so padding
 // slots pass their partner through unchanged, as the contract requires.
+// The arithmetic runs two columns per instruction (tile_reduce_x2), with
+// the scalar evaluation's bits.
 __device__ __forceinline__ MaxSum reduce_tile(float (&v)[kVocabTile], int ncols) {
     if (ncols < kVocabTile) {
 #pragma unroll
         for (int c = 0; c < kVocabTile; ++c)
             if (c >= ncols) v[c] = -CUDART_INF_F;
     }
-    // max is exact, so its evaluation order is free; four chains for ILP
-    float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+    uint64_t P[kVocabTile / 2];
 #pragma unroll
-    for (int c = 4; c < kVocabTile; c += 4) {
-        m0 = fmaxf(m0, v[c]);
-        m1 = fmaxf(m1, v[c + 1]);
-        m2 = fmaxf(m2, v[c + 2]);
-        m3 = fmaxf(m3, v[c + 3]);
-    }
-    const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-#pragma unroll
-    for (int c = 0; c < kVocabTile; ++c) v[c] = contract_exp(__fsub_rn(v[c], m));
-#pragma unroll
-    for (int w = kVocabTile / 2; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) v[i] = __fadd_rn(v[2 * i], v[2 * i + 1]);
-    }
-    MaxSum r;
-    r.m = m;
-    r.s = v[0];
-    return r;
+    for (int k = 0; k < kVocabTile / 2; ++k) P[k] = f2_pack(v[2 * k], v[2 * k + 1]);
+    return tile_reduce_x2(P);
 }
 
 // Backward epilogue: G[t, c] = bf16_RN(RN(g_t * d)) with d = RN(1 - p) at the
