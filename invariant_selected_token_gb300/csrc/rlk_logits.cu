@@ -75,23 +75,26 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
                                           int t, int c0, int ncols, bool valid, int64_t tl) {
     const float lse = valid ? a.lse[t] : 0.0f;
     const float gt = valid ? a.grad[t] : 0.0f;
+    const uint64_t neg_lse = f2_splat(-lse);  // RN(l - lse) = RN(l + (-lse))
+    const uint64_t g2 = f2_splat(gt);
     uint16_t* dst = a.G + static_cast<int64_t>(t) * a.ldG + c0;
 #pragma unroll
     for (int q = 0; q < kVocabTile / 8; ++q) {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            uint32_t pair = 0;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = q * 8 + i + h;
-                const float p = contract_exp(__fsub_rn(v[c], lse));
-                const float d = (c == tl) ? __fsub_rn(1.0f, p) : -p;
-                const float gv = valid ? __fmul_rn(gt, d) : 0.0f;
-                const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(gv));
-                pair |= b << (16 * h);
-            }
-            w[i / 2] = pair;
+        for (int i = 0; i < 4; ++i) {
+            // columns c, c + 1, two per instruction with the scalar bits
+            const int c = q * 8 + 2 * i;
+            float p0, p1;
+            f2_unpack(contract_exp_x2(f2_add(f2_pack(v[c], v[c + 1]), neg_lse)), p0, p1);
+            const float d0 = (c == tl) ? __fsub_rn(1.0f, p0) : -p0;
+            const float d1 = (c + 1 == tl) ? __fsub_rn(1.0f, p1) : -p1;
+            float g0, g1;
+            f2_unpack(f2_mul(g2, f2_pack(d0, d1)), g0, g1);
+            if (!valid) g0 = g1 = 0.0f;
+            const __nv_bfloat162 b = __floats2bfloat162_rn(g0, g1);  // round each to nearest
+            w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
+                   (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
         }
         if (q * 8 + 8 <= ncols) {
             *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
