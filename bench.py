@@ -45,12 +45,14 @@ def parse():
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode256",
-                            "logits_fp32", "logits_bf16", "backward", "grpo"],
+                            "logits_fp32", "logits_bf16", "backward", "grpo", "rmsnorm"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path; "
                         "backward: the deterministic backward of the packed batch; grpo: the "
-                        "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls)")
+                        "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls); "
+                        "rmsnorm: the strict RMSNorm (residual in and out) that produces the "
+                        "packed batch's hidden states")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -454,6 +456,76 @@ def grpo_arm(args, rank, world, dev, dist, W, binding, WL):
     return 0
 
 
+def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
+    """The strict RMSNorm producing the head's hidden states for the packed batch: residual
+    add (bf16 residual stream out) and normalisation, T = 4096, H = 4096.  Its four
+    [T, H] bf16 tensors (134 MB) are about L2's size, so L2 is flushed (a 512 MB write)
+    between timed calls, outside the timed interval."""
+    import torch
+    T = T_PACKED
+    g = torch.Generator(device=dev)
+    g.manual_seed(4242 + 1000 * rank)
+    x = (torch.randn((T, H), generator=g, device=dev) * 2.0).to(torch.bfloat16)
+    res = torch.randn((T, H), generator=g, device=dev).to(torch.bfloat16)
+    gamma = (1.0 + 0.1 * torch.randn((H,), generator=g, device=dev)).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    res_out = torch.empty_like(x)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        binding.rmsnorm(x, gamma, 1e-6, res, True, out, res_out, stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    for a, b in ev:
+        flush.fill_(1)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop(t0, time.time())
+    ms_total = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dist, dev)
+    call_ms = ms_total / K
+    peaks = load_peaks()
+    nbytes = float(4 * T * H * 2 + H * 2)
+    achieved = nbytes / (call_ms / 1000.0) / 1e9
+    if rank == 0:
+        out_line = {"metric": METRIC, "value": weak_scaling_value(world, T, K, ms_total),
+                    "unit": "tokens/s", "n_gpus": world, "steps": K,
+                    "warmup": max(3, args.warmup), "ms_per_step": call_ms,
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                    "dtype": "bf16", "data": "synthetic",
+                    "config": {"workload": "strict RMSNorm with residual add of the packed batch "
+                                           "(T=4096, H=4096, bf16 in/out, eps 1e-6)",
+                               "T": T, "H": H,
+                               "l2": "flushed between calls (512 MB write outside the timed "
+                                     "interval)"},
+                    "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                                 "peak_kind": "copy bandwidth (%s)" % peaks["source"],
+                                 "kernel": "k_rmsnorm", "kernel_ms": round(call_ms, 4),
+                                 "algorithmic": {"bytes": nbytes,
+                                                 "per_row": "read x, residual; write out, "
+                                                            "residual_out (4 x H x 2 B)"}},
+                    "cpu_baseline": None, "e2e": None, "gpu_launches": K, "clocks": clk,
+                    "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out_line))
+    return 0
+
+
 def backward_arm(args, rank, world, dev, dist, W, pk, binding):
     """grad_hidden and grad_W of sum_t g[t] logprob[t] for the packed batch."""
     import torch
@@ -540,6 +612,8 @@ def main():
         dist.barrier()
     binding.lib()
 
+    if args.workload == "rmsnorm":
+        return rmsnorm_arm(args, rank, world, dev, dist, binding, WL)
     W = WL.head_weights(dev)                       # same weights on every rank
     if args.workload == "grpo":
         return grpo_arm(args, rank, world, dev, dist, W, binding, WL)

@@ -291,6 +291,8 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
  *   out          device, bf16 [T][H]
  *   residual_out device, bf16 [T][H] receiving x' (the next residual stream), or NULL;
  *                requires residual
+ * out may be x and residual_out may be residual (updated in place): every
+ * element is read before it is written.  No other overlap is allowed.
  *   H            multiple of 64, at most 8192
  */
 rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma, float eps,

@@ -44,10 +44,109 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// kK column groups of 256 features per row (nextpow2(H) / 256, at least 1).
+constexpr int kRmsWarps = 4;
+
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    return pack_bf16(__fadd_rn(bf16_lo(a), bf16_lo(b)), __fadd_rn(bf16_hi(a), bf16_hi(b)));
+}
+
+// kK column groups of 256 features per row (nextpow2(H) / 256, 1 .. 16).
+// All of a row's loads are issued before any of its stores, so they are in
+// flight together.  out / residual_out may be x / residual themselves: every
+// element is read before the same element is written, and rows are disjoint.
+template <int kK>
+__global__ void __launch_bounds__(kRmsWarps * 32)
+    k_rmsnorm(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
+              int H, uint16_t* y, uint16_t* res_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * kRmsWarps;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kRmsWarps + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        uint4 v[kK];  // x' of this lane, 8 bf16 per group
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const int i0 = 256 * k + 8 * lane;
+            v[k] = i0 < H ? *reinterpret_cast<const uint4*>(x + t * H + i0) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (res) {
+            uint4 r[kK];
+#pragma unroll
+            for (int k = 0; k < kK; ++k) {
+                const int i0 = 256 * k + 8 * lane;
+                r[k] = i0 < H ? *reinterpret_cast<const uint4*>(res + t * H + i0)
+                              : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < kK; ++k) {
+                v[k].x = add_bf16x2(v[k].x, r[k].x);
+                v[k].y = add_bf16x2(v[k].y, r[k].y);
+                v[k].z = add_bf16x2(v[k].z, r[k].z);
+                v[k].w = add_bf16x2(v[k].w, r[k].w);
+            }
+            if (res_out) {
+#pragma unroll
+                for (int k = 0; k < kK; ++k) {
+                    const int i0 = 256 * k + 8 * lane;
+                    if (i0 < H) *reinterpret_cast<uint4*>(res_out + t * H + i0) = v[k];
+                }
+            }
+        }
+        float part[kK];
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            // levels 1-3: pairs (0,1),(2,3),(4,5),(6,7), then pairs of those; absent
+            // groups (i0 >= H) hold +0, which passes every partner through
+            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            float s2[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const float a = bf16_lo(w[p]), b = bf16_hi(w[p]);
+                s2[p] = __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
+            }
+            part[k] = __fadd_rn(__fadd_rn(s2[0], s2[1]), __fadd_rn(s2[2], s2[3]));
+        }
+        // levels 4-8 across lanes, lower lane on the left
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float other = __shfl_xor_sync(0xffffffffu, part[k], o);
+                part[k] = (lane & o) ? __fadd_rn(other, part[k]) : __fadd_rn(part[k], other);
+            }
+        }
+        // remaining levels over the column groups
+#pragma unroll
+        for (int w = kK / 2; w >= 1; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) part[i] = __fadd_rn(part[2 * i], part[2 * i + 1]);
+        }
+        const float mean = __fdiv_rn(part[0], static_cast<float>(H));
+        const float rstd = contract_rsqrt(__fadd_rn(mean, eps));
+        uint16_t* yr = y + t * H;
+#pragma unroll
+        for (int k = 0; k < kK; ++k) {
+            const int i0 = 256 * k + 8 * lane;
+            if (i0 < H) {
+                const uint4 g = *reinterpret_cast<const uint4*>(gamma + i0);
+                const uint32_t xw[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    o[p] = pack_bf16(__fmul_rn(__fmul_rn(bf16_lo(xw[p]), rstd), bf16_lo(gw[p])),
+                                     __fmul_rn(__fmul_rn(bf16_hi(xw[p]), rstd), bf16_hi(gw[p])));
+                *reinterpret_cast<uint4*>(yr + i0) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+// Rows wider than 4096 features (kK = 32): x and the residual of a row do
+// not fit in registers together, so the row is read group by group, each
+// group's residual store after its own loads.
 template <int kK>
 __global__ void __launch_bounds__(256)
-    k_rmsnorm(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
+    k_rmsnorm_grouped(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
               int H, uint16_t* y, uint16_t* res_out) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -122,10 +221,17 @@ __global__ void __launch_bounds__(256)
 
 template <int kK>
 cudaError_t launch_k(const RmsNormArgs& a, int num_sms, cudaStream_t stream) {
-    int64_t blocks = (static_cast<int64_t>(a.T) + 7) / 8;
-    if (blocks > static_cast<int64_t>(num_sms) * 16) blocks = static_cast<int64_t>(num_sms) * 16;
-    k_rmsnorm<kK><<<static_cast<int>(blocks), 256, 0, stream>>>(a.x, a.res, a.gamma, a.eps, a.T,
-                                                                  a.H, a.y, a.res_out);
+    if constexpr (kK <= 16) {
+        int64_t blocks = (static_cast<int64_t>(a.T) + kRmsWarps - 1) / kRmsWarps;
+        if (blocks > static_cast<int64_t>(num_sms) * 32) blocks = static_cast<int64_t>(num_sms) * 32;
+        k_rmsnorm<kK><<<static_cast<int>(blocks), kRmsWarps * 32, 0, stream>>>(
+            a.x, a.res, a.gamma, a.eps, a.T, a.H, a.y, a.res_out);
+    } else {
+        int64_t blocks = (static_cast<int64_t>(a.T) + 7) / 8;
+        if (blocks > static_cast<int64_t>(num_sms) * 16) blocks = static_cast<int64_t>(num_sms) * 16;
+        k_rmsnorm_grouped<kK><<<static_cast<int>(blocks), 256, 0, stream>>>(
+            a.x, a.res, a.gamma, a.eps, a.T, a.H, a.y, a.res_out);
+    }
     return cudaGetLastError();
 }
 

@@ -65,3 +65,22 @@ def test_rmsnorm_feeds_the_head(rlk, cuda_device):
     from oracle import linear_logprob as O
     ref_lp, _ = O.selected_logprob(bits_of(hidden), w.W, w.targets)
     assert np.abs(lp.cpu().numpy() - ref_lp).max() <= 1e-4
+
+
+@pytest.mark.parametrize("H", [4096, 8192, 320])
+def test_rmsnorm_in_place(rlk, cuda_device, H):
+    """out = x and residual_out = residual (the residual stream updated in place) give the
+    out-of-place bits."""
+    rng = np.random.default_rng(H + 11)
+    T = 37
+    x = bf16_dev(WL.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32) * 3), cuda_device)
+    r = bf16_dev(WL.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)), cuda_device)
+    g = bf16_dev(WL.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(H)).astype(np.float32)),
+                 cuda_device)
+    ref_out, ref_res = rlk.rmsnorm(x, g, 1e-6, r, want_residual_out=True)
+    xi, ri = x.clone(), r.clone()
+    out, r_out = rlk.rmsnorm(xi, g, 1e-6, ri, want_residual_out=True, out=xi, residual_out=ri)
+    torch.cuda.synchronize()
+    assert out.data_ptr() == xi.data_ptr() and r_out.data_ptr() == ri.data_ptr()
+    assert torch.equal(xi.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(ri.view(torch.int16), ref_res.view(torch.int16))
