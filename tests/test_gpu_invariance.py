@@ -173,3 +173,38 @@ def test_paired_and_single_cta_schedules_agree(rlk, cuda_device, monkeypatch, T,
     monkeypatch.delenv("RLK_TEST_PAIR")
     for a, b, name in zip(outs[0], outs[1], ("logprob", "lse", "grad_hidden", "grad_W")):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
+
+
+@pytest.mark.parametrize("T,H,V", [(1, 256, 5000), (300, 512, 20000)])
+def test_inputs_written_just_before_each_call(rlk, cuda_device, T, H, V):
+    """The logits and tile-tree kernels start early (programmatic dependent launch) and
+    wait for the previous kernel before touching memory.  Rewriting the inputs with an
+    ordinary kernel right before every call must still give each call the new inputs:
+    alternate two batches through the same buffers and compare every result, bit for
+    bit, with that batch's result computed alone."""
+    batches = [WL.to_device(WL.small_case(T, H, V, seed=s), cuda_device) for s in (31, 32)]
+    W = batches[0].W
+    ref = [rlk.linear_logprob(b.hidden, W, b.targets, None, 2) for b in batches]
+    ref_mat = [rlk.logits_logprob(rlk.debug_logits(b.hidden, W), b.targets, None, 2)
+               for b in batches]
+    g = torch.full((T,), 0.5, dtype=torch.float32, device=cuda_device)
+    ref_bwd = [rlk.linear_logprob_backward(b.hidden, W, b.targets, g, r[1], want_W=False)[0]
+               for b, r in zip(batches, ref)]
+    hidden = torch.empty_like(batches[0].hidden)
+    targets = torch.empty_like(batches[0].targets)
+    logits = torch.empty((T, V), dtype=torch.float32, device=cuda_device)
+    ws = rlk.new_workspace(T, V, 2, cuda_device)
+    lp = torch.empty(T, dtype=torch.float32, device=cuda_device)
+    lse = torch.empty_like(lp)
+    for it in range(12):
+        k = it % 2
+        hidden.copy_(batches[k].hidden)   # ordinary kernels, immediately before the call
+        targets.copy_(batches[k].targets)
+        rlk.linear_logprob(hidden, W, targets, None, 2, lp, lse, ws)
+        assert_same(lp, ref[k][0], "logprob, iteration %d" % it)
+        assert_same(lse, ref[k][1], "lse, iteration %d" % it)
+        logits.copy_(rlk.debug_logits(batches[k].hidden, W))
+        m_lp, m_lse = rlk.logits_logprob(logits, targets, None, 2)
+        assert_same(m_lp, ref_mat[k][0], "materialised logprob, iteration %d" % it)
+        gh, _ = rlk.linear_logprob_backward(hidden, W, targets, g, ref[k][1], want_W=False)
+        assert_same(gh, ref_bwd[k], "grad_hidden, iteration %d" % it)
