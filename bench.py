@@ -45,14 +45,16 @@ def parse():
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode256",
-                            "logits_fp32", "logits_bf16", "backward", "grpo", "rmsnorm"],
+                            "logits_fp32", "logits_bf16", "backward", "grpo", "rmsnorm",
+                            "sweep"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path; "
                         "backward: the deterministic backward of the packed batch; grpo: the "
                         "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls); "
                         "rmsnorm: the strict RMSNorm (residual in and out) that produces the "
-                        "packed batch's hidden states")
+                        "packed batch's hidden states; sweep: tokens/s against batch size on the "
+                        "8192-token sweep set")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()
@@ -456,6 +458,79 @@ def grpo_arm(args, rank, world, dev, dist, W, binding, WL):
     return 0
 
 
+SWEEP_SIZES = (1, 7, 64, 1024, 8192)
+
+
+def sweep_arm(args, rank, world, dev, dist, W, binding, WL):
+    """Tokens/s against batch size: the 8192-token sweep set cut into consecutive batches
+    of T rows (the last one ragged), each batch one rlk_tile_partials + rlk_tile_merge,
+    4 shards.  One step = one pass over all 8192 tokens at that T; `value` is the
+    T = 8192 point, the curve lists every T."""
+    import torch
+    sw = WL.sweep_set(W, dev, seed=1236 + 1000 * rank)
+    N = sw.hidden.shape[0]
+    ws = binding.new_workspace(max(SWEEP_SIZES), V, N_SHARDS, dev)
+    out_lp = torch.empty(N, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(N, dtype=torch.float32, device=dev)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+    curve = {}
+    clk = None
+    for T in SWEEP_SIZES:
+        batches = [(r0, min(N, r0 + T)) for r0 in range(0, N, T)]
+
+        def step():
+            for r0, r1 in batches:
+                binding.tile_partials(sw.hidden[r0:r1], W, sw.targets[r0:r1], None, N_SHARDS, ws,
+                                      status, stream)
+                binding.tile_merge(sw.targets[r0:r1], None, V, N_SHARDS, out_lp[r0:r1],
+                                   out_lse[r0:r1], ws, status, stream)
+
+        # a pass over 8192 tokens at T = 1 is 8192 calls: fewer steps for small T
+        K = max(1, min(args.steps, 8 if T < 64 else args.steps))
+        for _ in range(max(3, args.warmup) if T >= 64 else 1):
+            step()
+        torch.cuda.synchronize()
+        clocks = ClockSampler(int(str(dev).split(":")[-1]) if ":" in str(dev) else 0)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        c = clocks.stop(t0, time.time())
+        binding.raise_on_device_status(status)
+        ms = max_over_ranks(a.elapsed_time(b), dist, dev)
+        curve[str(T)] = {"tokens_per_s": weak_scaling_value(world, N, K, ms),
+                         "ms_per_pass": ms / K, "calls_per_pass": len(batches), "passes": K,
+                         "sm_mhz": (c or {}).get("sm_mhz")}
+        if T == max(SWEEP_SIZES):
+            clk, K_top, ms_top = c, K, ms
+    if rank == 0:
+        out = {"metric": METRIC, "value": curve[str(max(SWEEP_SIZES))]["tokens_per_s"],
+               "unit": "tokens/s", "n_gpus": world, "steps": K_top,
+               "warmup": max(3, args.warmup), "ms_per_step": ms_top / K_top,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": "sweep set: 8192 tokens (packed-batch distributions) in "
+                                      "consecutive batches of T rows, H=4096, V=151936, bf16, "
+                                      "4 vocab shards; value at T=8192",
+                          "sizes": list(SWEEP_SIZES), "H": H, "V": V, "n_shards": N_SHARDS,
+                          "l2": "inputs larger than L2 (W = 1.24 GB)",
+                          "parallelism": "dp%d (independent batches)" % world},
+               "curve": curve, "roofline": None, "cpu_baseline": None, "e2e": None,
+               "gpu_launches": 2 * K_top, "clocks": clk,
+               "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(out))
+    return 0
+
+
 def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
     """The strict RMSNorm producing the head's hidden states for the packed batch: residual
     add (bf16 residual stream out) and normalisation, T = 4096, H = 4096.  Its four
@@ -617,6 +692,8 @@ def main():
     W = WL.head_weights(dev)                       # same weights on every rank
     if args.workload == "grpo":
         return grpo_arm(args, rank, world, dev, dist, W, binding, WL)
+    if args.workload == "sweep":
+        return sweep_arm(args, rank, world, dev, dist, W, binding, WL)
     pk = WL.packed(W, dev, seed=rank_batch_seed(rank))  # each rank its own batch
     if args.workload.startswith("logits_"):
         return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
@@ -691,20 +768,23 @@ def main():
     # ---------------- end to end through the public call, host buffers
     e2e = None
     if not args.no_e2e:
-        h_hidden = hidden.cpu().pin_memory()
-        h_tg = targets.cpu().pin_memory()
-        h_lp = torch.empty(T, dtype=torch.float32).pin_memory()
-        h_lse = torch.empty(T, dtype=torch.float32).pin_memory()
-        d_hidden = torch.empty_like(hidden)
-        d_tg = torch.empty_like(targets)
+        # one pinned input buffer (hidden rows, then targets) and one output buffer
+        # (logprob, then lse): a single copy each way per step
+        hid_bytes = hidden.numel() * 2
+        h_in = torch.empty(hid_bytes + T * 4, dtype=torch.uint8).pin_memory()
+        h_in[:hid_bytes].view(torch.bfloat16).view(T, H).copy_(hidden.cpu())
+        h_in[hid_bytes:].view(torch.int32).copy_(targets.cpu())
+        h_out = torch.empty((2, T), dtype=torch.float32).pin_memory()
+        d_in = torch.empty(hid_bytes + T * 4, dtype=torch.uint8, device=dev)
+        d_hidden = d_in[:hid_bytes].view(torch.bfloat16).view(T, H)
+        d_tg = d_in[hid_bytes:].view(torch.int32)
+        d_out = torch.empty((2, T), dtype=torch.float32, device=dev)
 
         def e2e_step():
-            d_hidden.copy_(h_hidden, non_blocking=True)
-            d_tg.copy_(h_tg, non_blocking=True)
-            binding.linear_logprob(d_hidden, W, d_tg, None, N_SHARDS, out_lp, out_lse, ws, status,
-                                   stream)
-            h_lp.copy_(out_lp, non_blocking=True)
-            h_lse.copy_(out_lse, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            binding.linear_logprob(d_hidden, W, d_tg, None, N_SHARDS, d_out[0], d_out[1], ws,
+                                   status, stream)
+            h_out.copy_(d_out, non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -717,9 +797,12 @@ def main():
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
         e_ms = max_over_ranks(e_ms, dist, dev)
+        binding.raise_on_device_status(status)
+        assert torch.equal(h_out[0], out_lp.cpu()) and torch.equal(h_out[1], out_lse.cpu())
         e2e = {"value": weak_scaling_value(world, T, K, e_ms), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h_hidden.numel() * 2 + h_tg.numel() * 4),
-               "d2h_bytes_per_step": int(T * 4 * 2)}
+               "h2d_bytes_per_step": int(h_in.numel()),
+               "d2h_bytes_per_step": int(h_out.numel() * 4),
+               "copies_per_step": "one host-to-device, one device-to-host (pinned)"}
 
     # ---------------- roofline of the dominant kernel (logits GEMM + fused epilogue)
     peaks = load_peaks()
