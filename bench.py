@@ -182,12 +182,36 @@ def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, ms_total: f
     return world * tokens_per_rank * steps / (ms_total / 1000.0)
 
 
-def cpu_oracle_sample(hidden_bits, W_bits, targets, rows):
-    """Time the fp64 oracle on the listed rows; returns (seconds, rows)."""
+def cpu_oracle_sample(hidden_bits, W_bits, targets, rows, want_values=False):
+    """Time the fp64 oracle on the listed rows; returns (seconds, rows) and, with
+    want_values, also its (logprob, lse) for those rows."""
     from oracle import linear_logprob as oracle
     t0 = time.perf_counter()
-    oracle.selected_logprob(hidden_bits, W_bits, targets, rows=rows)
-    return time.perf_counter() - t0, (hidden_bits.shape[0] if rows is None else len(rows))
+    lp, lse = oracle.selected_logprob(hidden_bits, W_bits, targets, rows=rows)
+    took = time.perf_counter() - t0, (hidden_bits.shape[0] if rows is None else len(rows))
+    return took + (lp, lse) if want_values else took
+
+
+def hardware_fingerprint(dev):
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    driver = None
+    try:
+        driver = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader",
+                                 "-i", str(dev.index or 0)], capture_output=True, text=True,
+                                timeout=10).stdout.strip() or None
+    except Exception:
+        pass
+    return {"device": p.name, "sm_count": p.multi_processor_count,
+            "cc": "%d.%d" % (p.major, p.minor), "memory_gb": round(p.total_memory / 1e9, 1),
+            "driver": driver, "torch": torch.__version__}
+
+
+def diff_stats(d):
+    import numpy as np
+    d = np.asarray(d, dtype=np.float64)
+    return {"mean": float(d.mean()), "max": float(d.max()), "p50": float(np.percentile(d, 50)),
+            "p90": float(np.percentile(d, 90)), "p99": float(np.percentile(d, 99))}
 
 
 def reference_arm(args, rank, world):
@@ -828,15 +852,43 @@ def main():
                      "algorithmic": {"flops": flops, "bytes": nbytes}})
     step_roof_ms = max(t_tensor, t_hbm) * 1000.0
 
-    # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1)
+    # ---------------- invariance, live: sample rows recomputed as their own small batch
+    # (and, for a decode batch, the packed batch they came from) must give the timed
+    # run's outputs bit for bit
+    rows = WL.permutation(T, 4321)[:min(T, 24)]
+    rows_t = torch.from_numpy(rows).to(dev)
+    sub_lp, sub_lse = binding.linear_logprob(hidden[rows_t].contiguous(), W,
+                                             targets[rows_t].contiguous(), None, N_SHARDS)
+    pairs = [(sub_lp, out_lp[rows_t]), (sub_lse, out_lse[rows_t])]
+    layouts = ["%d-row batch of sample rows vs the timed T=%d batch" % (len(rows), T)]
+    if args.workload != "packed":
+        pk_lp, pk_lse = binding.linear_logprob(pk.hidden, W, pk.targets, None, N_SHARDS)
+        pairs += [(out_lp, pk_lp[idx]), (out_lse, pk_lse[idx])]
+        layouts.append("decode batch vs the same rows inside the packed T=4096 batch")
+    torch.cuda.synchronize()
+    mism = sum(int((a.view(torch.int32) != b.view(torch.int32)).sum().item()) for a, b in pairs)
+    maxd = max(float((a.double() - b.double()).abs().max().item()) for a, b in pairs)
+    invariance = {"mismatch_count": mism, "max_abs_diff": maxd, "compared": layouts}
+
+    # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1),
+    # whose values also give the parity of the timed run's outputs on those rows
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         W_bits = WL.bf16_tensor_bits(W)
-        rows = WL.permutation(T, 4321)[:min(T, 24)]
-        hid_bits = WL.bf16_tensor_bits(hidden[torch.from_numpy(rows).to(dev)])
-        s_, n_ = cpu_oracle_sample(hid_bits, W_bits, targets.cpu().numpy()[rows], None)
+        hid_bits = WL.bf16_tensor_bits(hidden[rows_t])
+        s_, n_, ref_lp, ref_lse = cpu_oracle_sample(hid_bits, W_bits, targets.cpu().numpy()[rows],
+                                                    None, want_values=True)
         cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": "%d rows of the batch over the full vocabulary (%.1f s)" % (n_, s_)}
+        got_lp = out_lp[rows_t].double().cpu().numpy()
+        got_lse = out_lse[rows_t].double().cpu().numpy()
+        d_lp = abs(got_lp - ref_lp)
+        d_lse = abs(got_lse - ref_lse) / abs(ref_lse)
+        parity = {"rows": int(n_), "logprob_abs_diff": diff_stats(d_lp),
+                  "lse_rel_diff_max": float(d_lse.max()),
+                  "tolerance": {"logprob_abs": 1e-4, "lse_rel": 2e-5},
+                  "within_tolerance": bool(d_lp.max() <= 1e-4 and d_lse.max() <= 2e-5)}
 
     if rank == 0:
         out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -850,6 +902,9 @@ def main():
                           "frac_of_step_roofline": round(step_roof_ms / ms_per_step, 4)},
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": 2 * K, "clocks": clk,
+               "active_tokens_per_step": T, "invariance": invariance, "parity": parity,
+               "peak_memory_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 3),
+               "hardware": hardware_fingerprint(dev),
                "contract": binding.contract_id(), "build": binding.build_fingerprint()}
         print(json.dumps(out))
     if dist is not None:
