@@ -625,7 +625,10 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
                                   dev->pair_clusters, st) != cudaSuccess)
         return RLK_ERR_CUDA;
 
-    // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum
+    // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum.
+    //    Feature tiles fastest: the CTAs running together share a few G slices (19 k
+    //    columns each) and cycle through W, rather than holding every token tile's G
+    //    slice at once (T = 8192: 4 % faster per step than token tiles fastest).
     if (grad_hidden) {
         CUtensorMap map_g, map_wmn;
         if ((s = encode_bf16_k_map(&map_g, G, V, T, ldG, kTileM)) != RLK_OK) return s;
@@ -643,6 +646,7 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
         g.kb_per_split = (kb + splits - 1) / splits;
         g.splits = (kb + g.kb_per_split - 1) / g.kb_per_split;
         g.vec_store = true;
+        g.n_fastest = true;
         g.status = dev_status;
         if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
             return RLK_ERR_CUDA;

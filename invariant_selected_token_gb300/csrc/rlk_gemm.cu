@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // work unit -> (split, n tile, m tile).  m fastest: CTAs running side by
     // side share one B slice through L2; n fastest: they share one A slice
-    // (grad_W, whose A -- the logit gradient -- is the large streamed operand).
+    // (both backward GEMMs, whose A -- the logit gradient -- is the large
+    // streamed operand).
     auto decode = [&](int unit, int& split, int& n_blk, int& m_blk) {
         split = unit / tiles_per_split;
         const int r = unit - split * tiles_per_split;
