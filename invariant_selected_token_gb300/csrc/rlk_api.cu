@@ -671,6 +671,10 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
         g.kb_per_split = g.k_blocks;
         g.splits = 1;
         g.vec_store = aligned(grad_W, 16);
+        // bands of hidden-feature tiles whose hidden columns take ~32 MB of L2
+        const int64_t band_bytes = int64_t(32) << 20;
+        const int64_t per_tile = T * 256 * 2;  // one 256-feature tile of the T hidden rows
+        g.n_band = int(band_bytes / per_tile > 1 ? band_bytes / per_tile : 1);
         g.n_fastest = true;
         g.status = dev_status;
         if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)

@@ -103,12 +103,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // side share one B slice through L2; n fastest: they share one A slice
     // (both backward GEMMs, whose A -- the logit gradient -- is the large
     // streamed operand).
+    // With n_band, the N tiles are taken in bands: every M tile visits a band's N
+    // tiles before the next band, so the band's B columns stay in L2 while A
+    // streams (grad_W at T = 8192: the hidden rows are 64 MB, two bands of 32 MB).
+    const int n_band = (g.n_band > 0 && g.n_band < num_n) ? g.n_band : num_n;
     auto decode = [&](int unit, int& split, int& n_blk, int& m_blk) {
         split = unit / tiles_per_split;
         const int r = unit - split * tiles_per_split;
         if (g.n_fastest) {
-            m_blk = r / num_n;
-            n_blk = r - m_blk * num_n;
+            const int full = num_m * n_band;  // units of a full band
+            const int band = r / full;
+            const int first_n = band * n_band;
+            const int nb = min(n_band, num_n - first_n);
+            const int within = r - band * full;
+            m_blk = within / nb;
+            n_blk = first_n + (within - m_blk * nb);
         } else {
             n_blk = r / num_m;
             m_blk = r - n_blk * num_m;

@@ -101,6 +101,8 @@ struct GemmArgs {
     int splits;
     bool vec_store;           // out rows 16-byte aligned
     bool n_fastest;           // raster: N tiles fastest (CTAs side by side share the A slice)
+    int n_band;               // n_fastest: N tiles per band (all M tiles visit a band's
+                              // N tiles before the next band); 0 = all N tiles
     int32_t* status;
 };
 
