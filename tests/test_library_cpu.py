@@ -94,6 +94,7 @@ def test_argument_validation_refuses_before_any_cuda_call(L):
     assert _call_full(L, T=-1) == 1
     assert _call_full(L, H=96) == 2
     assert _call_full(L, H=0) == 2
+    assert _call_full(L, H=(1 << 20) + 64) == 2  # beyond the widest hidden size served
     assert _call_full(L, V=262145) == 2
     assert _call_full(L, V=0) == 1
     assert _call_full(L, n_shards=3) == 2
