@@ -45,11 +45,12 @@ def parse():
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode256",
-                            "logits_fp32", "logits_bf16", "backward", "grpo", "rmsnorm",
-                            "sweep"],
+                            "logits_fp32", "logits_bf16", "log_softmax_fp32", "backward", "grpo",
+                            "rmsnorm", "sweep"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path; "
+                        "log_softmax_fp32: the full log_softmax [T, V] of those logits; "
                         "backward: the deterministic backward of the packed batch; grpo: the "
                         "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls); "
                         "rmsnorm: the strict RMSNorm (residual in and out) that produces the "
@@ -285,8 +286,15 @@ def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
     status = binding.new_status(dev)
     stream = torch.cuda.current_stream(dev)
 
+    full = args.workload == "log_softmax_fp32"
+    out_full = torch.empty((T, V), dtype=torch.float32, device=dev) if full else None
+    ws_full = binding.new_workspace(T, V, 1, dev) if full else None
+
     def step():
-        binding.logits_logprob(L, pk.targets, None, N_SHARDS, lp, lse, ws, status, stream)
+        if full:
+            binding.log_softmax(L, None, out_full, lse, ws_full, status, stream)
+        else:
+            binding.logits_logprob(L, pk.targets, None, N_SHARDS, lp, lse, ws, status, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -312,14 +320,18 @@ def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
     ms_total = max_over_ranks(ms_total, dist, dev)
     call_ms = ms_total / K
     nbytes = float(L.numel() * L.element_size())
+    if full:  # the logits are read twice (tile pairs, then the output pass); T x V written
+        nbytes = 3.0 * L.numel() * 4
     peaks = load_peaks()
-    sm_hz = (clk.get("sm_max_mhz") or 2070.0) * 1e6
+    sm_hz = ((clk or {}).get("sm_max_mhz") or 2070.0) * 1e6
     peak_ops = FMA_LANES_PER_SM * torch.cuda.get_device_properties(dev).multi_processor_count * sm_hz
     ops = FMA_OPS_PER_LOGIT * float(T) * V
     t_alu = ops / peak_ops
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     call_s = call_ms / 1000.0
-    common = {"kernel": "k_mat_tile_partials + k_tile_tree (whole call)", "traffic": None,
+    common = {"kernel": ("k_mat_tile_partials + k_tile_tree + k_log_softmax_out (whole call)"
+                         if full else "k_mat_tile_partials + k_tile_tree (whole call)"),
+              "traffic": None,
               "kernel_ms": round(call_ms, 4),
               "algorithmic": {"bytes": nbytes, "fma_ops": ops,
                               "fma_ops_per_logit": FMA_OPS_PER_LOGIT},
@@ -340,10 +352,12 @@ def materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL):
         out = {"metric": METRIC, "value": weak_scaling_value(world, T, K, ms_total),
                "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": max(3, args.warmup),
                "ms_per_step": call_ms, "higher_is_better": True, "scaling": "weak",
-               "vs_baseline": None, "dtype": "f32" if args.workload == "logits_fp32" else "bf16",
+               "vs_baseline": None, "dtype": "bf16" if args.workload == "logits_bf16" else "f32",
                "data": "synthetic",
-               "config": {"workload": "materialised logits of the packed batch (T=4096, "
-                                      "V=151936, %s), 4 vocab shards" % args.workload[7:],
+               "config": {"workload": ("full log_softmax [T, V] fp32 of the packed batch's "
+                                       "materialised fp32 logits (T=4096, V=151936)") if full else
+                                      ("materialised logits of the packed batch (T=4096, "
+                                       "V=151936, %s), 4 vocab shards" % args.workload[7:]),
                           "T": T, "V": V, "n_shards": N_SHARDS,
                           "l2": "inputs larger than L2 (logits %.2f GB)" % (nbytes / 1e9)},
                "roofline": roofline,
@@ -734,7 +748,7 @@ def main():
     if args.workload == "sweep":
         return sweep_arm(args, rank, world, dev, dist, W, binding, WL)
     pk = WL.packed(W, dev, seed=rank_batch_seed(rank))  # each rank its own batch
-    if args.workload.startswith("logits_"):
+    if args.workload.startswith("logits_") or args.workload == "log_softmax_fp32":
         return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
     if args.workload == "backward":
         return backward_arm(args, rank, world, dev, dist, W, pk, binding)
