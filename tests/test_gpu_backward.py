@@ -116,3 +116,27 @@ def test_qwen_shape_backward_sampled(rlk, qwen):
     ref_dW = G[:, vocab].T @ hd
     magW = np.abs(G[:, vocab]).T @ np.abs(hd)
     assert np.all(np.abs(dW.cpu().numpy()[vocab] - ref_dW) <= 2.0 ** -8 * magW + 1e-6)
+
+
+def test_grad_w_feature_bands(rlk, cuda_device):
+    """T = 8192 with H = 2560: grad_W takes its 10 feature tiles in bands (8, then a ragged
+    2), grad_hidden runs feature tiles fastest over 64 token tiles.  Both against the fp64
+    definition within the bf16 rounding of G, and grad_hidden rows against a 300-row
+    batch of the same tokens bit for bit."""
+    T, H, V = 8192, 2560, 1000
+    w = WL.small_case(T, H, V, seed=808, w_std=0.03)
+    dw = WL.to_device(w, cuda_device)
+    g_np = np.random.default_rng(8).standard_normal(T).astype(np.float32)
+    _, dh, dW, _ = run_backward(rlk, dw, torch.from_numpy(g_np).to(cuda_device))
+    L = O.logits(w.hidden, w.W)
+    G = O.grad_logits(L, w.targets, g_np.astype(np.float64))
+    Wd, h = bf16_to_f64(w.W), bf16_to_f64(w.hidden)
+    assert np.all(np.abs(dW.cpu().numpy() - G.T @ h) <= 2.0 ** -8 * (np.abs(G).T @ np.abs(h)) + 1e-6)
+    rows = np.arange(0, T, 97)
+    assert np.all(np.abs(dh.cpu().numpy()[rows] - G[rows] @ Wd)
+                  <= 2.0 ** -8 * (np.abs(G[rows]) @ np.abs(Wd)) + 1e-6)
+    lo, hi = 4000, 4300
+    sub = WL.DeviceWorkload("sub", dw.hidden[lo:hi].contiguous(), dw.W,
+                            dw.targets[lo:hi].contiguous())
+    _, dh_s, _, _ = run_backward(rlk, sub, torch.from_numpy(g_np[lo:hi]).to(cuda_device))
+    assert torch.equal(dh_s.view(torch.int32), dh[lo:hi].view(torch.int32))
