@@ -821,56 +821,66 @@ def main():
     # ---------------- end to end through the public call, host buffers
     e2e = None
     if not args.no_e2e:
-        # one pinned input buffer (hidden rows, then targets) and one output buffer
-        # (logprob, then lse): a single copy each way per step.  Two device input
-        # buffers: step k+1's inputs cross on a copy stream while step k computes.
+        # one pinned input buffer (hidden rows, then targets) and one pinned output buffer
+        # (logprob, then lse): a single copy each way per step.  Inputs and outputs are
+        # double-buffered on the device, uploads and read-backs run on their own
+        # streams: step k+1's upload and step k-1's read-back overlap step k.
         hid_bytes = hidden.numel() * 2
         h_in = torch.empty(hid_bytes + T * 4, dtype=torch.uint8).pin_memory()
         h_in[:hid_bytes].view(torch.bfloat16).view(T, H).copy_(hidden.cpu())
         h_in[hid_bytes:].view(torch.int32).copy_(targets.cpu())
         h_out = torch.empty((2, T), dtype=torch.float32).pin_memory()
         d_in = [torch.empty(hid_bytes + T * 4, dtype=torch.uint8, device=dev) for _ in range(2)]
-        d_out = torch.empty((2, T), dtype=torch.float32, device=dev)
-        copy_stream = torch.cuda.Stream(dev)
-        copied = [torch.cuda.Event() for _ in range(2)]
-        consumed = [torch.cuda.Event() for _ in range(2)]
-        for e in consumed:
+        d_out = [torch.empty((2, T), dtype=torch.float32, device=dev) for _ in range(2)]
+        up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        in_free = [torch.cuda.Event() for _ in range(2)]
+        computed = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        for e in in_free + out_free:
             e.record(stream)
         n_e2e = [0]
 
         def e2e_step():
             b = n_e2e[0] % 2
             n_e2e[0] += 1
-            copy_stream.wait_event(consumed[b])  # the step two back is done with this buffer
-            with torch.cuda.stream(copy_stream):
+            up_stream.wait_event(in_free[b])       # the step two back has read this input
+            with torch.cuda.stream(up_stream):
                 d_in[b].copy_(h_in, non_blocking=True)
-                copied[b].record(copy_stream)
-            stream.wait_event(copied[b])
+                uploaded[b].record(up_stream)
+            stream.wait_event(uploaded[b])
+            stream.wait_event(out_free[b])         # this output's previous read-back is done
             binding.linear_logprob(d_in[b][:hid_bytes].view(torch.bfloat16).view(T, H), W,
                                    d_in[b][hid_bytes:].view(torch.int32), None, N_SHARDS,
-                                   d_out[0], d_out[1], ws, status, stream)
-            consumed[b].record(stream)
-            h_out.copy_(d_out, non_blocking=True)
+                                   d_out[b][0], d_out[b][1], ws, status, stream)
+            in_free[b].record(stream)
+            computed[b].record(stream)
+            down_stream.wait_event(computed[b])
+            with torch.cuda.stream(down_stream):
+                h_out.copy_(d_out[b], non_blocking=True)
+                out_free[b].record(down_stream)
 
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        copy_stream.wait_event(e0)  # no copy of the timed steps starts before e0
+        up_stream.wait_event(e0)  # no copy of the timed steps starts before e0
         for _ in range(K):
             e2e_step()
+        for e in out_free:
+            stream.wait_event(e)  # the last read-backs are inside the timed region
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
         e_ms = max_over_ranks(e_ms, dist, dev)
         binding.raise_on_device_status(status)
-        assert torch.equal(h_out[0], out_lp.cpu()) and torch.equal(h_out[1], out_lse.cpu())
+        assert torch.equal(h_out[0], out_lp.cpu()) and torch.equal(h_out[1], out_lse.cpu())  # last step
         e2e = {"value": weak_scaling_value(world, T, K, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h_in.numel()),
                "d2h_bytes_per_step": int(h_out.numel() * 4),
-               "copies_per_step": "one host-to-device (on a copy stream, overlapping the "
-                                  "previous step's compute), one device-to-host (pinned)"}
+               "copies_per_step": "one host-to-device and one device-to-host (pinned), each on "
+                                  "its own stream, overlapping the neighbouring steps' compute"}
 
     # ---------------- roofline of the dominant kernel (logits GEMM + fused epilogue)
     peaks = load_peaks()
