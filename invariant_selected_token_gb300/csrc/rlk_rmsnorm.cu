@@ -45,6 +45,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 constexpr int kRmsWarps = 4;
+// Warps per row for rows of 512 .. 4096 features (measured at H = 4096, T =
+// 4096: one warp per row 38 us, two 33.6 us, four 27.3 us, eight 27.2 us).
+#ifndef RLK_RMS_TEAM
+#define RLK_RMS_TEAM 8
+#endif
 
 __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
     return pack_bf16(__fadd_rn(bf16_lo(a), bf16_lo(b)), __fadd_rn(bf16_hi(a), bf16_hi(b)));
@@ -141,45 +146,46 @@ __global__ void __launch_bounds__(kRmsWarps * 32)
     }
 }
 
-// kK = 2 .. 16: each row is split between the two warps of a pair, warp h
-// taking column groups [h kK/2, (h+1) kK/2) -- half the registers per lane,
-// so twice the rows in flight per SM.  The contract's tree over the column
-// groups is perfect, so its top level is exactly (left half) + (right half):
-// each warp forms its half as the one-warp kernel does, and the pair adds the
-// halves, left first, through shared memory (a named barrier per pair; two
-// slots alternate between rows, and a pair's warps are never more than one
-// row apart).
-constexpr int kPairsPerCta = 2;
+// kK = 2 .. 16: each row is split between kW warps (a team), warp w taking
+// column groups [w kK/kW, (w+1) kK/kW) -- fewer registers per lane, so more
+// rows in flight per SM.  The contract's tree over the column groups is
+// perfect, so its top log2(kW) levels combine the warps' sums pairwise in
+// order ((w0 + w1) + (w2 + w3) for four): each warp forms its part as the
+// one-warp kernel does, and the team combines the parts through shared
+// memory (a named barrier per team; two slots alternate between rows, and a
+// team's warps are never more than one row apart).
+__host__ __device__ constexpr int team_cta_threads(int kW) { return 32 * kW > 128 ? 32 * kW : 128; }
 
-template <int kK>
-__global__ void __launch_bounds__(kPairsPerCta * 64)
-    k_rmsnorm_pair(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
+template <int kK, int kW>
+__global__ void __launch_bounds__(team_cta_threads(kW))
+    k_rmsnorm_team(const uint16_t* x, const uint16_t* res, const uint16_t* gamma, float eps, int T,
                    int H, uint16_t* y, uint16_t* res_out) {
-    constexpr int kHalf = kK / 2;
-    __shared__ float halves[kPairsPerCta][2][2];  // [pair][slot][half]
+    constexpr int kTeams = team_cta_threads(kW) / (32 * kW);
+    constexpr int kPart = kK / kW;  // column groups per warp
+    __shared__ float parts[kTeams][2][kW];  // [team][slot][warp]
     const int lane = threadIdx.x & 31;
-    const int pair = threadIdx.x >> 6;
-    const int h = (threadIdx.x >> 5) & 1;
-    const int g0 = h * kHalf;  // first column group of this warp
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kPairsPerCta;
+    const int team = threadIdx.x / (32 * kW);
+    const int w = (threadIdx.x >> 5) % kW;
+    const int g0 = w * kPart;  // first column group of this warp
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTeams;
     int slot = 0;
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kPairsPerCta + pair; t < T; t += stride) {
-        uint4 v[kHalf];
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kTeams + team; t < T; t += stride) {
+        uint4 v[kPart];
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
+        for (int k = 0; k < kPart; ++k) {
             const int i0 = 256 * (g0 + k) + 8 * lane;
             v[k] = i0 < H ? *reinterpret_cast<const uint4*>(x + t * H + i0) : make_uint4(0u, 0u, 0u, 0u);
         }
         if (res) {
-            uint4 r[kHalf];
+            uint4 r[kPart];
 #pragma unroll
-            for (int k = 0; k < kHalf; ++k) {
+            for (int k = 0; k < kPart; ++k) {
                 const int i0 = 256 * (g0 + k) + 8 * lane;
                 r[k] = i0 < H ? *reinterpret_cast<const uint4*>(res + t * H + i0)
                               : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int k = 0; k < kHalf; ++k) {
+            for (int k = 0; k < kPart; ++k) {
                 v[k].x = add_bf16x2(v[k].x, r[k].x);
                 v[k].y = add_bf16x2(v[k].y, r[k].y);
                 v[k].z = add_bf16x2(v[k].z, r[k].z);
@@ -187,26 +193,26 @@ __global__ void __launch_bounds__(kPairsPerCta * 64)
             }
             if (res_out) {
 #pragma unroll
-                for (int k = 0; k < kHalf; ++k) {
+                for (int k = 0; k < kPart; ++k) {
                     const int i0 = 256 * (g0 + k) + 8 * lane;
                     if (i0 < H) *reinterpret_cast<uint4*>(res_out + t * H + i0) = v[k];
                 }
             }
         }
-        float part[kHalf];
+        float part[kPart];
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
-            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        for (int k = 0; k < kPart; ++k) {
+            const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
             float s2[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-                const float a = bf16_lo(w[p]), b = bf16_hi(w[p]);
+                const float a = bf16_lo(q[p]), b = bf16_hi(q[p]);
                 s2[p] = __fadd_rn(__fmul_rn(a, a), __fmul_rn(b, b));
             }
             part[k] = __fadd_rn(__fadd_rn(s2[0], s2[1]), __fadd_rn(s2[2], s2[3]));
         }
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
+        for (int k = 0; k < kPart; ++k) {
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float other = __shfl_xor_sync(0xffffffffu, part[k], o);
@@ -214,19 +220,26 @@ __global__ void __launch_bounds__(kPairsPerCta * 64)
             }
         }
 #pragma unroll
-        for (int w = kHalf / 2; w >= 1; w >>= 1) {
+        for (int n = kPart / 2; n >= 1; n >>= 1) {
 #pragma unroll
-            for (int i = 0; i < w; ++i) part[i] = __fadd_rn(part[2 * i], part[2 * i + 1]);
+            for (int i = 0; i < n; ++i) part[i] = __fadd_rn(part[2 * i], part[2 * i + 1]);
         }
-        if (lane == 0) halves[pair][slot][h] = part[0];
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-        const float total = __fadd_rn(halves[pair][slot][0], halves[pair][slot][1]);
+        if (lane == 0) parts[team][slot][w] = part[0];
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * kW) : "memory");
+        float p[kW];
+#pragma unroll
+        for (int i = 0; i < kW; ++i) p[i] = parts[team][slot][i];
+#pragma unroll
+        for (int n = kW / 2; n >= 1; n >>= 1) {
+#pragma unroll
+            for (int i = 0; i < n; ++i) p[i] = __fadd_rn(p[2 * i], p[2 * i + 1]);
+        }
         slot ^= 1;
-        const float mean = __fdiv_rn(total, static_cast<float>(H));
+        const float mean = __fdiv_rn(p[0], static_cast<float>(H));
         const float rstd = contract_rsqrt(__fadd_rn(mean, eps));
         uint16_t* yr = y + t * H;
 #pragma unroll
-        for (int k = 0; k < kHalf; ++k) {
+        for (int k = 0; k < kPart; ++k) {
             const int i0 = 256 * (g0 + k) + 8 * lane;
             if (i0 < H) {
                 const uint4 g = *reinterpret_cast<const uint4*>(gamma + i0);
@@ -234,9 +247,9 @@ __global__ void __launch_bounds__(kPairsPerCta * 64)
                 const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
                 uint32_t o[4];
 #pragma unroll
-                for (int p = 0; p < 4; ++p)
-                    o[p] = pack_bf16(__fmul_rn(__fmul_rn(bf16_lo(xw[p]), rstd), bf16_lo(gw[p])),
-                                     __fmul_rn(__fmul_rn(bf16_hi(xw[p]), rstd), bf16_hi(gw[p])));
+                for (int q = 0; q < 4; ++q)
+                    o[q] = pack_bf16(__fmul_rn(__fmul_rn(bf16_lo(xw[q]), rstd), bf16_lo(gw[q])),
+                                     __fmul_rn(__fmul_rn(bf16_hi(xw[q]), rstd), bf16_hi(gw[q])));
                 *reinterpret_cast<uint4*>(yr + i0) = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
@@ -324,9 +337,11 @@ __global__ void __launch_bounds__(256)
 template <int kK>
 cudaError_t launch_k(const RmsNormArgs& a, int num_sms, cudaStream_t stream) {
     if constexpr (kK >= 2 && kK <= 16) {
-        int64_t blocks = (static_cast<int64_t>(a.T) + kPairsPerCta - 1) / kPairsPerCta;
+        constexpr int kW = (kK >= RLK_RMS_TEAM) ? RLK_RMS_TEAM : kK;  // warps per row
+        constexpr int kTeams = team_cta_threads(kW) / (32 * kW);
+        int64_t blocks = (static_cast<int64_t>(a.T) + kTeams - 1) / kTeams;
         if (blocks > static_cast<int64_t>(num_sms) * 32) blocks = static_cast<int64_t>(num_sms) * 32;
-        k_rmsnorm_pair<kK><<<static_cast<int>(blocks), kPairsPerCta * 64, 0, stream>>>(
+        k_rmsnorm_team<kK, kW><<<static_cast<int>(blocks), team_cta_threads(kW), 0, stream>>>(
             a.x, a.res, a.gamma, a.eps, a.T, a.H, a.y, a.res_out);
     } else if constexpr (kK <= 16) {
         int64_t blocks = (static_cast<int64_t>(a.T) + kRmsWarps - 1) / kRmsWarps;
