@@ -170,13 +170,15 @@ bool use_pair(int64_t T, const DeviceState* dev) {
     return pair && T > kTileM && dev->pair_clusters >= 1;
 }
 
-// RLK_TEST_DROP_STAGE=1: CTA 0's producer skips its first pipeline stage, so
-// its MMA wait runs out (bounded) and the kernel reports RLK_ERR_TIMEOUT --
-// the failure-detection test's way to exercise the give-up path.
-bool test_drop_stage() {
+// RLK_TEST_DROP_STAGE=1 (the logits kernel) or 2 (the grad_hidden GEMM): CTA
+// 0's producer skips its first pipeline stage, so its MMA wait runs out
+// (bounded) and the kernel reports RLK_ERR_TIMEOUT -- the failure-detection
+// tests' way to exercise the give-up path.
+int test_drop_stage_code() {
     const char* f = std::getenv("RLK_TEST_DROP_STAGE");
-    return f && std::atoi(f) != 0;
+    return f ? std::atoi(f) : 0;
 }
+bool test_drop_stage() { return test_drop_stage_code() == 1; }
 
 rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t* targets,
                                const uint8_t* active, int64_t T, int64_t H, int64_t V_local,
@@ -647,6 +649,7 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
         g.splits = (kb + g.kb_per_split - 1) / g.kb_per_split;
         g.vec_store = true;
         g.n_fastest = true;
+        g.test_drop_stage = test_drop_stage_code() == 2 ? 1 : 0;
         g.status = dev_status;
         if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
             return RLK_ERR_CUDA;

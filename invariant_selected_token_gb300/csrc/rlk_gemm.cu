@@ -127,6 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
+            if (g.test_drop_stage && blockIdx.x == 0) {
+                // test only: leave stage 0 unfilled; the MMA's bounded wait gives up
+                stage = 1;
+            }
             for (int unit = blockIdx.x; unit < total && !*abort_flag; unit += gridDim.x) {
                 int split, n_blk, m_blk;
                 decode(unit, split, n_blk, m_blk);

@@ -103,6 +103,7 @@ struct GemmArgs {
     bool n_fastest;           // raster: N tiles fastest (CTAs side by side share the A slice)
     int n_band;               // n_fastest: N tiles per band (all M tiles visit a band's
                               // N tiles before the next band); 0 = all N tiles
+    int test_drop_stage;      // test only: CTA 0 never loads its first stage (wait runs out)
     int32_t* status;
 };
 

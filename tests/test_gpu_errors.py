@@ -111,3 +111,33 @@ def test_pipeline_wait_gives_up_with_timeout_status(rlk, cuda_device, monkeypatc
     rlk.raise_on_device_status(status2)
     ref_lp, _ = O.selected_logprob(w.hidden, w.W, w.targets)
     assert np.abs(lp.cpu().numpy() - ref_lp).max() <= 1e-4
+
+
+def test_gemm_pipeline_wait_gives_up_with_timeout_status(rlk, cuda_device, monkeypatch):
+    """The backward's grad_hidden GEMM with a pipeline stage that never fills: its bounded
+    wait gives up, RLK_ERR_TIMEOUT is reported, the kernel returns, and the next backward
+    on the same context gives the reference bits."""
+    import time
+    w = WL.small_case(256, 256, 3000, seed=13, w_std=0.05)
+    dw = WL.to_device(w, cuda_device)
+    _, lse = rlk.linear_logprob(dw.hidden, dw.W, dw.targets)
+    g = torch.full((256,), 0.5, dtype=torch.float32, device=cuda_device)
+    ref_dh, ref_dW = rlk.linear_logprob_backward(dw.hidden, dw.W, dw.targets, g, lse)
+    torch.cuda.synchronize()
+    monkeypatch.setenv("RLK_TEST_DROP_STAGE", "2")
+    status = rlk.new_status(cuda_device)
+    t0 = time.time()
+    rlk.linear_logprob_backward(dw.hidden, dw.W, dw.targets, g, lse, status=status)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    monkeypatch.delenv("RLK_TEST_DROP_STAGE")
+    with pytest.raises(rlk.RlkError) as e:
+        rlk.raise_on_device_status(status)
+    assert e.value.code == rlk.RLK_ERR_TIMEOUT
+    assert elapsed < 30
+    status2 = rlk.new_status(cuda_device)
+    dh, dW = rlk.linear_logprob_backward(dw.hidden, dw.W, dw.targets, g, lse, status=status2)
+    torch.cuda.synchronize()
+    rlk.raise_on_device_status(status2)
+    assert torch.equal(dh.view(torch.int32), ref_dh.view(torch.int32))
+    assert torch.equal(dW.view(torch.int32), ref_dW.view(torch.int32))
