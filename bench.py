@@ -234,7 +234,9 @@ def reference_arm(args, rank, world):
         hid_bits = WL.bf16_tensor_bits(WL.rms_hidden(T_PACKED, H, dev, 1234))
         tg = np.random.default_rng(1234).integers(0, V, T_PACKED).astype(np.int32)
     W_bits = WL.bf16_tensor_bits(W)
-    rows_per_step = 16
+    # a bounded sample: about 2400 rows in all (~2 minutes on 16 host cores), at most
+    # 16 and at least 1 per step
+    rows_per_step = max(1, min(16, 2400 // max(1, args.steps)))
     rng = np.random.default_rng(4321)
     for _ in range(args.warmup):
         cpu_oracle_sample(hid_bits, W_bits, tg, rng.choice(T_PACKED, 2, replace=False))
