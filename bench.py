@@ -234,9 +234,12 @@ def reference_arm(args, rank, world):
         hid_bits = WL.bf16_tensor_bits(WL.rms_hidden(T_PACKED, H, dev, 1234))
         tg = np.random.default_rng(1234).integers(0, V, T_PACKED).astype(np.int32)
     W_bits = WL.bf16_tensor_bits(W)
-    # a bounded sample: about 2400 rows in all (~2 minutes on 16 host cores), at most
-    # 16 and at least 1 per step
-    rows_per_step = max(1, min(16, 2400 // max(1, args.steps)))
+    # A bounded sample per step.  Each oracle call first decodes all of W to fp64
+    # (~0.7 s on 16 host cores), so rows are taken in batches large enough for the
+    # call to be mostly dot products: 64 rows per step at the default 300 steps
+    # (~4 minutes), up to 512 for shorter runs.
+    K = max(1, args.steps)
+    rows_per_step = 64 if K >= 100 else min(512, max(64, 6400 // K))
     rng = np.random.default_rng(4321)
     for _ in range(args.warmup):
         cpu_oracle_sample(hid_bits, W_bits, tg, rng.choice(T_PACKED, 2, replace=False))
@@ -485,7 +488,7 @@ def grpo_arm(args, rank, world, dev, dist, W, binding, WL):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         act_rows = torch.nonzero(g.active).flatten().cpu().numpy()
-        rows = act_rows[WL.permutation(len(act_rows), 4321)[:24]]
+        rows = act_rows[WL.permutation(len(act_rows), 4321)[:2048]]
         W_bits = WL.bf16_tensor_bits(W)
         hid_bits = WL.bf16_tensor_bits(g.hidden[torch.from_numpy(rows).to(dev)])
         s_, n_ = cpu_oracle_sample(hid_bits, W_bits, g.targets.cpu().numpy()[rows], None)
@@ -911,7 +914,7 @@ def main():
     # ---------------- invariance, live: sample rows recomputed as their own small batch
     # (and, for a decode batch, the packed batch they came from) must give the timed
     # run's outputs bit for bit
-    rows = WL.permutation(T, 4321)[:min(T, 24)]
+    rows = WL.permutation(T, 4321)[:min(T, 2048)]
     rows_t = torch.from_numpy(rows).to(dev)
     sub_lp, sub_lse = binding.linear_logprob(hidden[rows_t].contiguous(), W,
                                              targets[rows_t].contiguous(), None, N_SHARDS)
