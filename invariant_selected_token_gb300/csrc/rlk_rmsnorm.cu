@@ -10,12 +10,19 @@
 //   rstd = rlk_rsqrt(a)
 //   y_i  = bf16_RN(RN(RN(x'_i * rstd) * gamma_i))
 //
-// One warp per row.  Element i = 256 k + 8 l + j is lane l's j-th value of
-// column group k, so each lane reads 16 contiguous bytes per group (the warp
-// reads 512 contiguous bytes) and the tree's levels fall as: 1-3 over j
-// inside the lane, 4-8 over l across lanes (xor 1..16, lower lane on the
-// left), the rest over k inside the lane -- the contract's pairwise tree
-// over the feature index, whatever the row's position in the batch.
+// Layout: element i = 256 k + 8 l + j is lane l's j-th value of column group
+// k, so each lane reads 16 contiguous bytes per group (a warp reads 512
+// contiguous bytes) and the tree's levels fall as: 1-3 over j inside the
+// lane, 4-8 over l across lanes (xor 1..16, lower lane on the left), then
+// over the groups -- the contract's pairwise tree over the feature index,
+// whatever the row's position in the batch.  Three kernels share it:
+//   k_rmsnorm          one warp per row (rows of at most 256 features);
+//   k_rmsnorm_team     rows of 512 .. 4096 features split across a team of
+//                      warps, each holding whole groups; the team's partial
+//                      sums are the top levels of the same tree;
+//   k_rmsnorm_grouped  one warp per row, group by group (rows wider than 4096
+//                      features, whose x and residual do not fit in
+//                      registers together).
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
