@@ -210,6 +210,27 @@ rlk_status_t rlk_debug_logits(const void* hidden, const void* W, int64_t T, int6
                               float* out_logits, int32_t* dev_status, rlk_stream_t stream);
 
 /*
+ * Diagnostic: evaluates one of the contract's primitives on the GPU over the
+ * fp32 bit patterns [first, first + count) and writes
+ *   sum_i (bits(f(x_i)) + 0x9E3779B9) * (2 i + 1)   (mod 2^64)
+ * to *out_hash, so a caller can compare the device's primitive with another
+ * implementation of the contract over a whole input range (any single
+ * differing output changes the sum).  The primitives are the contract's
+ * fixed exp, log and rsqrt ("vLLM RL-Kernel v0.1.0: ROCm 上でのビット単位の
+ * トレーニング-ロールアウト一貫性", section 数値実行契約, item 6: the math
+ * primitives are part of the contract); the check itself has no counterpart
+ * in the pages.
+ *   which     0: rlk_exp; 1: rlk_exp evaluated two values per instruction (the
+ *             kernels' packed form; must equal 0); 2: rlk_log; 3: rlk_rsqrt
+ *   first, count  first bit pattern and how many; first + count <= 2^32
+ *   out_hash  device, one uint64_t, overwritten
+ * Errors: RLK_ERR_INVALID_ARG for an unknown primitive, a range beyond 2^32
+ * or a null out_hash; otherwise as the other calls.
+ */
+rlk_status_t rlk_debug_primitive_hash(int which, uint32_t first, uint64_t count,
+                                      uint64_t* out_hash, rlk_stream_t stream);
+
+/*
  * Selected-token logprob from logits that already exist in memory, under
  * the same contract (the blog's rl_kernel.log_softmax with a fixed reduction
  * tree, sections 4.2-4.3, read at the target).  Given the fp32 logits the

@@ -29,7 +29,8 @@ EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rl
             "rlk_workspace_size", "rlk_linear_logprob", "rlk_linear_logprob_shard",
             "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
             "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax",
-            "rlk_backward_workspace_size", "rlk_linear_logprob_backward", "rlk_rmsnorm"]
+            "rlk_backward_workspace_size", "rlk_linear_logprob_backward", "rlk_rmsnorm",
+            "rlk_debug_primitive_hash"]
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.rlk_rmsnorm.argtypes = [P, P, P, ctypes.c_float, i64, i64, P, P, P]
         L.rlk_log_softmax.restype = i32
         L.rlk_log_softmax.argtypes = [P, i32, i64, P, i64, i64, P, P, P, sz, P, P]
+        L.rlk_debug_primitive_hash.restype = i32
+        L.rlk_debug_primitive_hash.argtypes = [i32, ctypes.c_uint32, ctypes.c_uint64, P, P]
         _lib = L
     return _lib
 
@@ -373,3 +376,16 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
                              _ptr(residual_out if want_residual_out else None),
                              _stream(dev, stream)), "rlk_rmsnorm")
     return out, (residual_out if want_residual_out else None)
+
+
+PRIMITIVES = {"exp": 0, "exp_x2": 1, "log": 2, "rsqrt": 3}
+
+
+def primitive_hash(which: str, first: int, count: int, device, stream=None) -> int:
+    """Position-weighted 64-bit sum of one contract primitive over fp32 bit patterns
+    [first, first + count), evaluated on the device (see rlk_debug_primitive_hash)."""
+    out = torch.zeros(1, dtype=torch.int64, device=device)
+    _check(lib().rlk_debug_primitive_hash(PRIMITIVES[which], first, count, _ptr(out),
+                                          _stream(torch.device(device), stream)),
+           "rlk_debug_primitive_hash")
+    return int(out.item()) & ((1 << 64) - 1)

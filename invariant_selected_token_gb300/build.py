@@ -25,7 +25,7 @@ LIB = os.path.join(HERE, "librlk.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["rlk_logits.cu", "rlk_logits_mat.cu", "rlk_merge.cu", "rlk_gemm.cu", "rlk_rmsnorm.cu",
-           "rlk_api.cu", "rlk_static_ws.cu"]
+           "rlk_api.cu", "rlk_static_ws.cu", "rlk_debug.cu"]
 HEADERS = ["rlk_ptx.cuh", "rlk_contract.cuh", "rlk_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

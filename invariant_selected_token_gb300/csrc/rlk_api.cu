@@ -715,4 +715,18 @@ rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma,
                : RLK_ERR_CUDA;
 }
 
+rlk_status_t rlk_debug_primitive_hash(int which, uint32_t first, uint64_t count,
+                                      uint64_t* out_hash, rlk_stream_t stream) {
+    if (which < 0 || which > 3 || !out_hash) return RLK_ERR_INVALID_ARG;
+    if (uint64_t(first) + count > (uint64_t(1) << 32)) return RLK_ERR_INVALID_ARG;
+    if (!aligned(out_hash, 8)) return RLK_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    rlk_status_t s = device_check(&dev);
+    if (s != RLK_OK) return s;
+    return rlk::launch_primitive_hash(which, first, count, out_hash, dev->sm_count,
+                                      reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RLK_OK
+               : RLK_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -126,6 +126,11 @@ struct RmsNormArgs {
 
 cudaError_t launch_rmsnorm(const RmsNormArgs& a, int num_sms, cudaStream_t stream);
 
+// Position-weighted hash of a contract primitive over fp32 bit patterns
+// [first, first + count): which 0 exp, 1 exp two lanes at a time, 2 log, 3 rsqrt.
+cudaError_t launch_primitive_hash(int which, uint32_t first, uint64_t count, uint64_t* out,
+                                  int num_sms, cudaStream_t stream);
+
 struct ShardMergeArgs {
     const rlk_partial_t* parts[RLK_MAX_SHARDS];
     int n_shards;

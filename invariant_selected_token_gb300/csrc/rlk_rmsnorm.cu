@@ -27,22 +27,12 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "rlk_contract.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
 namespace {
 
-// rsqrt(a) for positive normal a: Lomont's seed for the bit-level inverse
-// square-root estimate, two Newton steps, then one in correction form.
-// Under 0.86 ulp over [2^-40, 2^40] (checked exhaustively on the CPU).
-__device__ __forceinline__ float contract_rsqrt(float a) {
-    float y = __uint_as_float(0x5f375a86u - (__float_as_uint(a) >> 1));
-    const float h = __fmul_rn(0.5f, a);
-#pragma unroll
-    for (int k = 0; k < 2; ++k) y = __fmul_rn(y, __fmaf_rn(-h, __fmul_rn(y, y), 1.5f));
-    const float e = __fmaf_rn(-h, __fmul_rn(y, y), 0.5f);
-    return __fmaf_rn(y, e, y);
-}
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

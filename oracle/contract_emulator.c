@@ -486,3 +486,19 @@ void emu_rsqrt_sweep(float lo, float hi, double* max_ulp, float* worst_x, int64_
     *worst_x = wx;
     *count = cnt;
 }
+
+/* Position-weighted sum of a primitive over the fp32 bit patterns
+ * [first, first + count): sum_i (bits(f(x_i)) + 0x9E3779B9) (2 i + 1) mod 2^64,
+ * with which 0 or 1: emu_exp, 2: emu_log, 3: emu_rsqrt -- the same sum the
+ * library's diagnostic forms on the GPU, where 1 is its two-lane exp. */
+uint64_t emu_primitive_hash(int which, uint32_t first, uint64_t count) {
+    init_constants();
+    uint64_t h = 0;
+#pragma omp parallel for reduction(+ : h) schedule(static)
+    for (int64_t i = 0; i < (int64_t)count; ++i) {
+        const float x = u2f(first + (uint32_t)i);
+        const float y = which <= 1 ? emu_exp(x) : which == 2 ? emu_log(x) : emu_rsqrt(x);
+        h += ((uint64_t)f2u(y) + 0x9E3779B9ull) * (2ull * (uint64_t)i + 1ull);
+    }
+    return h;
+}

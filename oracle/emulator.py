@@ -56,12 +56,21 @@ def lib():
         L.emu_rmsnorm.argtypes = [P, P, P, f, i64, i64, P, P]
         L.emu_constants.restype = None
         L.emu_constants.argtypes = [P]
+        L.emu_primitive_hash.restype = ctypes.c_uint64
+        L.emu_primitive_hash.argtypes = [i32, ctypes.c_uint32, ctypes.c_uint64]
         _lib = L
     return _lib
 
 
 def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data
+
+
+def primitive_hash(which: str, first: int, count: int) -> int:
+    """sum_i (bits(f(x_i)) + 0x9E3779B9) (2 i + 1) mod 2^64 over the fp32 bit patterns
+    [first, first + count) for f = exp ("exp" and "exp_x2"), log or rsqrt."""
+    code = {"exp": 0, "exp_x2": 1, "log": 2, "rsqrt": 3}[which]
+    return int(lib().emu_primitive_hash(code, first, count))
 
 
 def exp(x: float) -> np.float32:
