@@ -174,30 +174,37 @@ __global__ void __launch_bounds__(kMatWarps * 32, 3)
     void* sm = reinterpret_cast<uint8_t*>(mat_smem) +
                warp * (kSliceTiles * Pitch<kDtype>::value * kElem);
     const int slices_per_row = (n_tiles + kSliceTiles - 1) / kSliceTiles;
-    const int64_t n_tasks = static_cast<int64_t>(T) * slices_per_row;
+    // The warp's tasks are (row t, slice s of 32 tiles) in row-major order,
+    // every gridDim.x * kMatWarps-th one; the position advances by a fixed
+    // (rows, slices) step instead of dividing a task index per task.
+    // Inactive rows are skipped.
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kMatWarps;
-    // the warp's tasks (row t, slice of 32 tiles), inactive rows skipped
-    auto next_active = [&](int64_t task) {
-        while (task < n_tasks && active && active[task / slices_per_row] == 0) task += stride;
-        return task;
+    const int step_t = static_cast<int>(stride / slices_per_row);
+    const int step_s = static_cast<int>(stride - static_cast<int64_t>(step_t) * slices_per_row);
+    auto advance = [&](int& t, int& s) {
+        t += step_t;
+        s += step_s;
+        if (s >= slices_per_row) {
+            s -= slices_per_row;
+            ++t;
+        }
     };
-    auto issue = [&](int64_t task) {
-        const int t = static_cast<int>(task / slices_per_row);
-        const int64_t c0 = (task - static_cast<int64_t>(t) * slices_per_row) *
-                           static_cast<int64_t>(kSliceTiles * kVocabTile);
+    auto skip_inactive = [&](int& t, int& s) {
+        while (t < T && active && active[t] == 0) advance(t, s);
+    };
+    auto issue = [&](int t, int s) {
+        const int64_t c0 = static_cast<int64_t>(s) * (kSliceTiles * kVocabTile);
         const int ncols_total = min(kSliceTiles * kVocabTile, V - static_cast<int>(c0));
         const void* row = static_cast<const uint8_t*>(logits) + static_cast<int64_t>(t) * ld * kElem;
         stage_issue<kDtype>(row, c0, ncols_total, lane, vec, sm);
     };
-    int64_t task = next_active(static_cast<int64_t>(blockIdx.x) * kMatWarps + warp);
-    if (task < n_tasks) issue(task);
-    // Software pipeline: the slice is copied into registers (one tile per
-    // lane), the next slice's copies are issued into the freed buffer, and
-    // the reduction runs while they are in flight.
-    while (task < n_tasks) {
+    const int first = static_cast<int>(blockIdx.x) * kMatWarps + warp;
+    int t = first / slices_per_row, s = first - (first / slices_per_row) * slices_per_row;
+    skip_inactive(t, s);
+    if (t < T) issue(t, s);
+    while (t < T) {
         stage_wait();
-        const int t = static_cast<int>(task / slices_per_row);
-        const int j = static_cast<int>(task - static_cast<int64_t>(t) * slices_per_row) * kSliceTiles + lane;
+        const int j = s * kSliceTiles + lane;
         const bool own = j < n_tiles;
         const int ncols = own ? min(kVocabTile, V - j * kVocabTile) : 0;
         uint64_t P[64];
@@ -209,8 +216,10 @@ __global__ void __launch_bounds__(kMatWarps * 32, 3)
             read_tile_pairs<kDtype>(sm, lane, P);
         }
         __syncwarp();  // every lane has its tile: the buffer is free
-        const int64_t next = next_active(task + stride);
-        if (next < n_tasks) issue(next);
+        int nt = t, ns = s;
+        advance(nt, ns);
+        skip_inactive(nt, ns);
+        if (nt < T) issue(nt, ns);
         if (own) {
             // columns past the vocabulary are not part of the tile: -inf, whose
             // exp is +0, so their tree partners pass through unchanged
@@ -226,7 +235,8 @@ __global__ void __launch_bounds__(kMatWarps * 32, 3)
             const MaxSum r = tile_reduce_x2(P);
             partials[static_cast<int64_t>(t) * n_tiles + j] = make_float2(r.m, r.s);
         }
-        task = next;
+        t = nt;
+        s = ns;
     }
 }
 
