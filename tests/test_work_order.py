@@ -5,7 +5,10 @@ unit) in bands of 32 token tiles, vocabulary-major inside a band; the GEMM's
 ``decode`` in ``csrc/rlk_gemm.cu`` takes N tiles in bands when ``n_band`` is
 set.  Each must visit every tile exactly once (a skipped or repeated tile
 would leave logits unreduced or reduce them twice), and the bands must come
-in order with every tile of a band before the next.
+in order with every tile of a band before the next.  The materialised-logits
+kernel (``csrc/rlk_logits_mat.cu``) walks each warp's (row, slice) tasks by a
+fixed (rows, slices) step; together the warps must take every slice of every
+active row exactly once and no slice of an inactive row.
 """
 import pytest
 
@@ -54,3 +57,49 @@ def test_gemm_units_cover_every_tile_once_band_by_band():
                 nb = n_band if 0 < n_band < num_n else num_n
                 bands = [n // nb for _, n in seq]
                 assert bands == sorted(bands)
+
+
+def mat_walk(first, T, slices_per_row, stride, active):
+    """One warp's (row, slice) tasks, stepped as the kernel steps them."""
+    step_t, step_s = stride // slices_per_row, stride % slices_per_row
+
+    def advance(t, s):
+        t, s = t + step_t, s + step_s
+        if s >= slices_per_row:
+            s, t = s - slices_per_row, t + 1
+        return t, s
+
+    def skip_inactive(t, s):
+        while t < T and active is not None and not active[t]:
+            t, s = advance(t, s)
+        return t, s
+
+    t, s = skip_inactive(first // slices_per_row, first % slices_per_row)
+    out = []
+    while t < T:
+        out.append((t, s))
+        t, s = skip_inactive(*advance(t, s))
+    return out
+
+
+@pytest.mark.parametrize("masked", [False, True])
+def test_mat_walk_takes_every_active_slice_once(masked):
+    warps_per_cta = 4
+    for T in (1, 2, 5, 37, 300):
+        active = [(t * 7 + 3) % 5 != 0 for t in range(T)] if masked else None
+        for slices_per_row in (1, 2, 3, 38, 75):
+            n_tasks = T * slices_per_row
+            for ctas in (1, 3, 152, 456, 760):
+                blocks = min(ctas, (n_tasks + warps_per_cta - 1) // warps_per_cta)
+                stride = blocks * warps_per_cta
+                seen = []
+                for first in range(stride):
+                    walk = mat_walk(first, T, slices_per_row, stride, active)
+                    # row-major task order, every stride-th task from `first`
+                    tasks = [t * slices_per_row + s for t, s in walk]
+                    assert all(b - a >= stride and (b - first) % stride == 0
+                               for a, b in zip(tasks, tasks[1:]))
+                    seen += walk
+                want = [(t, s) for t in range(T) for s in range(slices_per_row)
+                        if active is None or active[t]]
+                assert sorted(seen) == want
