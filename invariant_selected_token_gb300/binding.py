@@ -100,6 +100,12 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on(device):
+    """Make the tensors' device current for the call: the library launches on the calling
+    thread's current device."""
+    return torch.cuda.device(device)
+
+
 def _stream(device: torch.device, stream) -> ctypes.c_void_p:
     s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -184,28 +190,31 @@ def linear_logprob(hidden: torch.Tensor, W: torch.Tensor, targets: torch.Tensor,
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, V, n_shards, dev)
-    _check(lib().rlk_linear_logprob(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H, V,
-                                    n_shards, _ptr(out_logprob), _ptr(out_lse), _ptr(workspace),
-                                    workspace.numel(), _ptr(status), _stream(dev, stream)),
-           "rlk_linear_logprob")
+    with _on(dev):
+        _check(lib().rlk_linear_logprob(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H, V,
+                                        n_shards, _ptr(out_logprob), _ptr(out_lse), _ptr(workspace),
+                                        workspace.numel(), _ptr(status), _stream(dev, stream)),
+               "rlk_linear_logprob")
     return out_logprob, out_lse
 
 
 def tile_partials(hidden, W, targets, active, n_shards, workspace, status=None, stream=None):
     dev = hidden.device
     T, H = hidden.shape
-    _check(lib().rlk_tile_partials(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H,
-                                   W.shape[0], n_shards, _ptr(workspace), workspace.numel(),
-                                   _ptr(status), _stream(dev, stream)), "rlk_tile_partials")
+    with _on(dev):
+        _check(lib().rlk_tile_partials(_ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H,
+                                       W.shape[0], n_shards, _ptr(workspace), workspace.numel(),
+                                       _ptr(status), _stream(dev, stream)), "rlk_tile_partials")
 
 
 def tile_merge(targets, active, V, n_shards, out_logprob, out_lse, workspace, status=None,
                stream=None):
     dev = targets.device
     T = targets.shape[0]
-    _check(lib().rlk_tile_merge(_ptr(targets), _ptr(active), T, V, n_shards, _ptr(out_logprob),
-                                _ptr(out_lse), _ptr(workspace), workspace.numel(), _ptr(status),
-                                _stream(dev, stream)), "rlk_tile_merge")
+    with _on(dev):
+        _check(lib().rlk_tile_merge(_ptr(targets), _ptr(active), T, V, n_shards, _ptr(out_logprob),
+                                    _ptr(out_lse), _ptr(workspace), workspace.numel(), _ptr(status),
+                                    _stream(dev, stream)), "rlk_tile_merge")
 
 
 def workspace_records(workspace: torch.Tensor, T: int, V: int, n_shards: int) -> torch.Tensor:
@@ -233,10 +242,12 @@ def linear_logprob_shard(hidden, W_shard, targets, active, V_total: int, n_shard
         out = torch.empty((T, 4), dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, ve - vb, 1, dev)
-    _check(lib().rlk_linear_logprob_shard(_ptr(hidden), _ptr(W_shard), _ptr(targets),
-                                          _ptr(active), T, H, V_total, n_shards, shard, _ptr(out),
-                                          _ptr(workspace), workspace.numel(), _ptr(status),
-                                          _stream(dev, stream)), "rlk_linear_logprob_shard")
+    with _on(dev):
+        _check(lib().rlk_linear_logprob_shard(_ptr(hidden), _ptr(W_shard), _ptr(targets),
+                                              _ptr(active), T, H, V_total, n_shards, shard,
+                                              _ptr(out),
+                                              _ptr(workspace), workspace.numel(), _ptr(status),
+                                              _stream(dev, stream)), "rlk_linear_logprob_shard")
     return out
 
 
@@ -252,9 +263,10 @@ def lse_merge(partials: Sequence[torch.Tensor], active=None, out_logprob=None, o
         out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
     if out_lse is None:
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
-    _check(lib().rlk_lse_merge(ctypes.cast(arr, ctypes.c_void_p), n, T, _ptr(active),
-                               _ptr(out_logprob), _ptr(out_lse), _ptr(status),
-                               _stream(dev, stream)), "rlk_lse_merge")
+    with _on(dev):
+        _check(lib().rlk_lse_merge(ctypes.cast(arr, ctypes.c_void_p), n, T, _ptr(active),
+                                   _ptr(out_logprob), _ptr(out_lse), _ptr(status),
+                                   _stream(dev, stream)), "rlk_lse_merge")
     return out_logprob, out_lse
 
 
@@ -265,8 +277,9 @@ def debug_logits(hidden: torch.Tensor, W: torch.Tensor, status=None, stream=None
     T, H = hidden.shape
     V = W.shape[0]
     out = torch.empty((T, V), dtype=torch.float32, device=dev)
-    _check(lib().rlk_debug_logits(_ptr(hidden), _ptr(W), T, H, V, _ptr(out), _ptr(status),
-                                  _stream(dev, stream)), "rlk_debug_logits")
+    with _on(dev):
+        _check(lib().rlk_debug_logits(_ptr(hidden), _ptr(W), T, H, V, _ptr(out), _ptr(status),
+                                      _stream(dev, stream)), "rlk_debug_logits")
     return out
 
 
@@ -297,10 +310,12 @@ def logits_logprob(logits: torch.Tensor, targets: torch.Tensor, active=None, n_s
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, V, n_shards, dev)
-    _check(lib().rlk_logits_logprob(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(targets),
-                                    _ptr(active), T, V, n_shards, _ptr(out_logprob), _ptr(out_lse),
-                                    _ptr(workspace), workspace.numel(), _ptr(status),
-                                    _stream(dev, stream)), "rlk_logits_logprob")
+    with _on(dev):
+        _check(lib().rlk_logits_logprob(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(targets),
+                                        _ptr(active), T, V, n_shards, _ptr(out_logprob),
+                                        _ptr(out_lse),
+                                        _ptr(workspace), workspace.numel(), _ptr(status),
+                                        _stream(dev, stream)), "rlk_logits_logprob")
     return out_logprob, out_lse
 
 
@@ -315,9 +330,10 @@ def log_softmax(logits: torch.Tensor, active=None, out=None, out_lse=None, works
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
     if workspace is None:
         workspace = new_workspace(T, V, 1, dev)
-    _check(lib().rlk_log_softmax(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(active), T, V,
-                                 _ptr(out), _ptr(out_lse), _ptr(workspace), workspace.numel(),
-                                 _ptr(status), _stream(dev, stream)), "rlk_log_softmax")
+    with _on(dev):
+        _check(lib().rlk_log_softmax(_ptr(logits), DTYPES[logits.dtype], ld, _ptr(active), T, V,
+                                     _ptr(out), _ptr(out_lse), _ptr(workspace), workspace.numel(),
+                                     _ptr(status), _stream(dev, stream)), "rlk_log_softmax")
     return out, out_lse
 
 
@@ -350,11 +366,13 @@ def linear_logprob_backward(hidden, W, targets, grad_logprob, lse, active=None,
     if workspace is None:
         workspace = torch.empty(max(256, backward_workspace_size(T, H, V)), dtype=torch.uint8,
                                 device=dev)
-    _check(lib().rlk_linear_logprob_backward(
-        _ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), _ptr(grad_logprob), _ptr(lse), T, H, V,
-        _ptr(grad_hidden if want_hidden else None), _ptr(grad_W if want_W else None),
-        _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
-        "rlk_linear_logprob_backward")
+    with _on(dev):
+        _check(lib().rlk_linear_logprob_backward(
+            _ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), _ptr(grad_logprob), _ptr(lse),
+            T, H, V,
+            _ptr(grad_hidden if want_hidden else None), _ptr(grad_W if want_W else None),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
+            "rlk_linear_logprob_backward")
     return (grad_hidden if want_hidden else None), (grad_W if want_W else None)
 
 
@@ -372,9 +390,10 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-6,
         out = torch.empty_like(x)
     if want_residual_out and residual_out is None:
         residual_out = torch.empty_like(x)
-    _check(lib().rlk_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
-                             _ptr(residual_out if want_residual_out else None),
-                             _stream(dev, stream)), "rlk_rmsnorm")
+    with _on(dev):
+        _check(lib().rlk_rmsnorm(_ptr(x), _ptr(residual), _ptr(gamma), float(eps), T, H, _ptr(out),
+                                 _ptr(residual_out if want_residual_out else None),
+                                 _stream(dev, stream)), "rlk_rmsnorm")
     return out, (residual_out if want_residual_out else None)
 
 
@@ -385,7 +404,8 @@ def primitive_hash(which: str, first: int, count: int, device, stream=None) -> i
     """Position-weighted 64-bit sum of one contract primitive over fp32 bit patterns
     [first, first + count), evaluated on the device (see rlk_debug_primitive_hash)."""
     out = torch.zeros(1, dtype=torch.int64, device=device)
-    _check(lib().rlk_debug_primitive_hash(PRIMITIVES[which], first, count, _ptr(out),
-                                          _stream(torch.device(device), stream)),
-           "rlk_debug_primitive_hash")
+    with _on(torch.device(device)):
+        _check(lib().rlk_debug_primitive_hash(PRIMITIVES[which], first, count, _ptr(out),
+                                              _stream(torch.device(device), stream)),
+               "rlk_debug_primitive_hash")
     return int(out.item()) & ((1 << 64) - 1)
