@@ -48,7 +48,9 @@
  *     for an active row whose target no shard owns (that row's outputs are
  *     NaN), RLK_ERR_TIMEOUT if a pipeline wait ran out (outputs undefined;
  *     the kernel returns instead of hanging).
- *   - T == 0 is a no-op returning RLK_OK.
+ *   - T == 0 is a no-op returning RLK_OK; T < 0 or T > RLK_MAX_ROWS returns
+ *     RLK_ERR_INVALID_ARG (kernels index rows in 32 bits and step past
+ *     the last row by less than 2^20).
  *   - Inactive rows (active_mask[t] == 0) give out_logprob = out_lse = 0 and
  *     all-zero partial records; their hidden row and target are never used
  *     in any other row's result.  active_mask == NULL means all active.
@@ -92,6 +94,7 @@ typedef struct rlk_partial {
 #define RLK_MAX_SHARDS 8
 #define RLK_MAX_VOCAB 262144          /* 2048 tiles */
 #define RLK_K_BLOCK 64                /* H must be a multiple of this */
+#define RLK_MAX_ROWS 2146435072       /* 2^31 - 2^20: the largest T (rows) any call takes */
 #define RLK_DTYPE_F32 0               /* logits element types for the materialised-logits calls */
 #define RLK_DTYPE_BF16 1
 

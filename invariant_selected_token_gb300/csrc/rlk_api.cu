@@ -267,7 +267,7 @@ BackwardLayout backward_layout_of(int64_t T, int64_t H, int64_t V) {
 
 rlk_status_t common_checks(const void* hidden, const void* W, const int32_t* targets, int64_t T,
                            int64_t H) {
-    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     if (T > 0 && (!hidden || !W || !targets)) return RLK_ERR_INVALID_ARG;
     if (H < rlk::kBlockK || H % rlk::kBlockK != 0 || H > (int64_t(1) << 20)) return RLK_ERR_UNSUPPORTED;
     if (!aligned(hidden, 16) || !aligned(W, 16) || !aligned(targets, 4)) return RLK_ERR_ALIGNMENT;
@@ -313,7 +313,7 @@ rlk_status_t run_tile_tree(const int32_t* targets, const uint8_t* active, int64_
 
 // Checks shared by the two materialised-logits calls.
 rlk_status_t mat_checks(const void* logits, int dtype, int64_t ld, int64_t T, int64_t V) {
-    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     if (V < 1 || ld < V) return RLK_ERR_INVALID_ARG;
     if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
     if (dtype != RLK_DTYPE_F32 && dtype != RLK_DTYPE_BF16) return RLK_ERR_UNSUPPORTED;
@@ -363,7 +363,7 @@ rlk_status_t rlk_shard_range(int64_t V, int n_shards, int shard, int64_t* v_begi
 }
 
 size_t rlk_workspace_size(int64_t T, int64_t V, int n_shards) {
-    if (T < 0 || shard_check(V, n_shards) != RLK_OK) return 0;
+    if (T < 0 || T > RLK_MAX_ROWS || shard_check(V, n_shards) != RLK_OK) return 0;
     return layout_of(T, V, n_shards).total;
 }
 
@@ -392,7 +392,7 @@ rlk_status_t rlk_tile_merge(const int32_t* targets, const uint8_t* active_mask, 
                             int64_t V, int n_shards, float* out_logprob, float* out_lse,
                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
                             rlk_stream_t stream) {
-    if (T < 0 || T > INT32_MAX - kTileM) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     rlk_status_t s = shard_check(V, n_shards);
     if (s != RLK_OK) return s;
     if (T == 0) return RLK_OK;
@@ -471,7 +471,7 @@ rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
 rlk_status_t rlk_lse_merge(const rlk_partial_t* const* partials, int n_shards, int64_t T,
                            const uint8_t* active_mask, float* out_logprob, float* out_lse,
                            int32_t* dev_status, rlk_stream_t stream) {
-    if (T < 0 || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     if (n_shards < 1 || n_shards > RLK_MAX_SHARDS || log2_exact(n_shards) < 0)
         return RLK_ERR_UNSUPPORTED;
     if (T == 0) return RLK_OK;
@@ -572,7 +572,9 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
 }
 
 size_t rlk_backward_workspace_size(int64_t T, int64_t H, int64_t V) {
-    if (T < 0 || H < rlk::kBlockK || H % rlk::kBlockK != 0 || V < 1 || V > RLK_MAX_VOCAB) return 0;
+    if (T < 0 || T > RLK_MAX_ROWS || H < rlk::kBlockK || H % rlk::kBlockK != 0 || V < 1 ||
+        V > RLK_MAX_VOCAB)
+        return 0;
     return backward_layout_of(T, H, V).total;
 }
 
@@ -689,7 +691,7 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
 rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma, float eps,
                          int64_t T, int64_t H, void* out, void* residual_out,
                          rlk_stream_t stream) {
-    if (T < 0 || T > INT32_MAX) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     if (H < 64 || H % 64 != 0 || H > 8192) return RLK_ERR_UNSUPPORTED;
     if (!(eps > 0.0f) || !(eps < 3.0e38f)) return RLK_ERR_INVALID_ARG;
     if (T == 0) return RLK_OK;

@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(kMatWarps * 32, 3)
     // The warp's tasks are (row t, slice s of 32 tiles) in row-major order,
     // every gridDim.x * kMatWarps-th one; the position advances by a fixed
     // (rows, slices) step instead of dividing a task index per task.
-    // Inactive rows are skipped.
+    // Inactive rows are skipped.  The row index stays in 32 bits: T is at most
+    // RLK_MAX_ROWS = 2^31 - 2^20 and a step passes the last row by less than
+    // one grid stride (far below 2^20 tasks).
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kMatWarps;
     const int step_t = static_cast<int>(stride / slices_per_row);
     const int step_s = static_cast<int>(stride - static_cast<int64_t>(step_t) * slices_per_row);

@@ -66,7 +66,7 @@ extern "C" rlk_status_t rlk_linear_logprob_static_ws(
     int64_t T, int64_t H, int64_t V, int n_shards, float* out_logprob, float* out_lse,
     int32_t* dev_status, rlk_stream_t stream) {
     if (T == 0) return RLK_OK;
-    if (T < 0) return RLK_ERR_INVALID_ARG;
+    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
     const size_t need = rlk_workspace_size(T, V, n_shards);
     if (need == 0) {
         // invalid V / n_shards: let the stage report the precise code

@@ -17,6 +17,9 @@ from invariant_selected_token_gb300 import binding, build
 from oracle import linear_logprob as O
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+# the largest row count any call takes, as include/rlk.h defines it
+MAX_ROWS = int(re.search(r"#define RLK_MAX_ROWS (\d+)",
+                         open(os.path.join(ROOT, "include", "rlk.h")).read()).group(1))
 
 
 @pytest.fixture(scope="module")
@@ -105,6 +108,8 @@ def test_argument_validation_refuses_before_any_cuda_call(L):
     assert _call_full(L, ws_bytes=100) == 4
     assert _call_full(L, ws=None) == 1
     assert _call_full(L, T=0) == 0                    # empty batch: no-op
+    assert _call_full(L, T=MAX_ROWS + 1) == 1         # beyond the largest row count
+    assert L.rlk_workspace_size(MAX_ROWS + 1, 1000, 1) == 0
     # shard variant and merge
     assert L.rlk_linear_logprob_shard(0x10000, 0x20000, 0x30000, None, 4, 64, 1000, 4, 4, 0x40000,
                                       0x60000, 1 << 20, None, None) == 1
@@ -136,6 +141,7 @@ def test_materialised_logits_validation(L):
     assert call(targets=None) == 1
     assert call(wsb=10) == 4
     assert call(T=0) == 0
+    assert call(T=MAX_ROWS + 1) == 1
     g = L.rlk_log_softmax
     assert g(0x10000, 0, 1024, None, 4, 1000, None, 0x50000, 0x60000, 1 << 20, None, None) == 1
     assert g(0x10001, 0, 1001, None, 4, 1000, 0x40000, 0x50000, 0x60000, 1 << 20, None, None) == 3
@@ -151,3 +157,5 @@ def test_rmsnorm_validation(L):
     assert f(0x10000, None, 0x20000, C.c_float(1e-6), 4, 4096, 0x30000, 0x40000, None) == 1
     assert f(0x10008, None, 0x20000, C.c_float(1e-6), 4, 4096, 0x30000, None, None) == 3
     assert f(0x10000, None, 0x20000, C.c_float(1e-6), 0, 4096, 0x30000, None, None) == 0
+    assert f(0x10000, None, 0x20000, C.c_float(1e-6), MAX_ROWS + 1, 4096, 0x30000, None,
+             None) == 1
