@@ -73,8 +73,8 @@ typedef struct CUstream_st* rlk_stream_t;
 
 typedef enum rlk_status {
     RLK_OK = 0,
-    RLK_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad shard index */
-    RLK_ERR_UNSUPPORTED = 2,   /* device not sm_103; H % 64 != 0; V > 262144; n_shards not in {1,2,4,8} or > tiles */
+    RLK_ERR_INVALID_ARG = 1,   /* null pointer, negative size, T > RLK_MAX_ROWS, bad shard index */
+    RLK_ERR_UNSUPPORTED = 2,   /* device not sm_103; H % 64 != 0 or H > 2^20; V > 262144; n_shards not in {1,2,4,8} or > tiles */
     RLK_ERR_ALIGNMENT = 3,     /* hidden/W not 16-byte aligned, workspace not 256-byte aligned */
     RLK_ERR_WORKSPACE = 4,     /* workspace smaller than rlk_workspace_size() */
     RLK_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (launch, device query) */
@@ -136,7 +136,7 @@ size_t rlk_workspace_size(int64_t T, int64_t V, int n_shards);
  *   W            device, bf16 [V][H] row-major (vocabulary rows), 16-byte aligned
  *   targets      device, int32 [T], global vocabulary ids
  *   active_mask  device, uint8 [T] (nonzero = active) or NULL
- *   H            multiple of 64
+ *   H            multiple of 64, at most 2^20
  *   V            1 .. RLK_MAX_VOCAB
  *   n_shards     1, 2, 4 or 8, and at most ceil(V / 128)
  *   out_logprob  device, float [T];  out_lse  device, float [T]
@@ -242,9 +242,10 @@ rlk_status_t rlk_debug_primitive_hash(int which, uint32_t first, uint64_t count,
  *   logits       device, [T][ld] row-major, elements RLK_DTYPE_F32 or RLK_DTYPE_BF16
  *                (bf16 widens exactly to fp32); only columns [0, V) are read
  *   ld           row stride in elements, >= V; logits aligned to their element
- *                size (rows that start on 16-byte (fp32) / 8-byte (bf16)
- *                boundaries, i.e. ld % 4 == 0 on an aligned base, are read with
- *                vector loads; the values and results are the same either way)
+ *                size (when every row starts on a 16-byte boundary -- a 16-byte
+ *                aligned base and ld * element size a multiple of 16 -- rows
+ *                are copied in 16-byte pieces; the values and results are the
+ *                same either way)
  *   workspace    >= rlk_workspace_size(T, V, n_shards) bytes, same layout as rlk_linear_logprob
  * Other arguments, outputs and errors as rlk_linear_logprob.
  */
