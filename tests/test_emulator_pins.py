@@ -153,3 +153,27 @@ def test_inactive_and_unowned_rows():
     assert np.all(out["rec_owned"][:, 1] == 0) and np.all(out["rec_s"][:, 1] == 0)
     assert np.isnan(out["logprob"][2]) and np.isnan(out["lse"][2])
     assert np.isfinite(out["logprob"][3])
+
+
+@pytest.mark.parametrize("which,first,count", [("exp", 0xC2000000, 3000), ("exp", 0x80000000, 700),
+                                               ("exp_x2", 0xC1000000, 700), ("log", 0x3F800000, 2000),
+                                               ("log", 0x49FFF000, 700), ("rsqrt", 0x2B800000, 700),
+                                               ("rsqrt", 0x3F000000, 2000)])
+def test_primitive_hash_is_the_documented_sum(which, first, count):
+    """The emulator's range hash (the GPU's is compared against it) is
+    sum_i (bits(f(x_i)) + 0x9E3779B9) (2 i + 1) mod 2^64 of the scalar primitive
+    over the bit patterns first + i: recomputed here one input at a time."""
+    f = {"exp": E.exp, "exp_x2": E.exp, "log": E.log, "rsqrt": E.rsqrt}[which]
+    xs = np.arange(first, first + count, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    bits = [int(np.array([f(float(x))], dtype=np.float32).view(np.uint32)[0]) for x in xs]
+
+    def fold(bs):
+        return sum((b + 0x9E3779B9) * (2 * i + 1) for i, b in enumerate(bs)) % (1 << 64)
+
+    assert fold(bits) == E.primitive_hash(which, first, count)
+    # the weights are odd, hence invertible mod 2^64: any one output changed
+    # (by less than 2^32) changes the sum
+    for i in (0, count // 3, count - 1):
+        changed = list(bits)
+        changed[i] ^= 1
+        assert fold(changed) != fold(bits)
