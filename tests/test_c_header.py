@@ -5,7 +5,7 @@ import subprocess
 
 import pytest
 
-from invariant_selected_token_gb300 import binding, build
+from invariant_selected_token_gb300 import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 

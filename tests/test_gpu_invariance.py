@@ -5,7 +5,6 @@ A token's logprob and lse must not depend on the batch it is computed in
 (few rows) versus a packed launch, or on the run.  Every comparison is on
 the uint32 views: mismatch_count = 0 and max_abs_diff = 0.
 """
-import numpy as np
 import pytest
 import torch
 

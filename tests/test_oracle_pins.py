@@ -4,7 +4,6 @@ The second half copies the oracle module, plants one plausible mistake in
 the copy (on the CPU) and checks that at least one pin fails for it.
 """
 import importlib.util
-import types
 
 import numpy as np
 import pytest
