@@ -8,10 +8,17 @@ every negative fp32 down to -inf (the contract only forms arguments <= 0),
 both as the scalar function and in the two-lane packed form the kernels use;
 log on [1, 2^21] (every root sum of a tile tree); rsqrt on [2^-40, 2^40].
 NaN inputs are outside the contract's domain and not compared.
+
+A second opinion on accuracy: on a strided sample of each range, the contract's
+values (the emulator's, which the device equals bit for bit) lie within 3 ulp of
+CUDA's own expf / logf / rsqrtf as torch evaluates them on the device (each side
+is within 2 ulp of the true value).
 """
 import functools
 
+import numpy as np
 import pytest
+import torch
 
 from oracle import emulator as E
 
@@ -48,3 +55,25 @@ def test_hash_sees_a_shifted_range(rlk, cuda_device):
     assert a != b
     assert a == E.primitive_hash("exp", 0xBF000000, 1 << 20)
     assert b == E.primitive_hash("exp", 0xBF000001, 1 << 20)
+
+
+SAMPLES = {  # (first bit pattern, last, the emulator's scalar function, torch's)
+    "exp": (0xC2AC0000, 0x80000001, E.exp, torch.exp),       # [-86, -2^-149]
+    "log": (0x3F800000, 0x4A000000, E.log, torch.log),       # [1, 2^21]
+    "rsqrt": (0x2B800000, 0x53800000, E.rsqrt, torch.rsqrt),  # [2^-40, 2^40]
+}
+
+
+@pytest.mark.parametrize("which", sorted(SAMPLES))
+def test_primitives_within_3_ulp_of_cuda_math(cuda_device, which):
+    lo, hi, contract, cuda_fn = SAMPLES[which]
+    a, b = min(lo, hi), max(lo, hi)
+    bits = np.unique(np.concatenate([np.linspace(a, b, 1 << 17).astype(np.uint32),
+                                     np.array([a, b], dtype=np.uint32)]))
+    x = bits.view(np.float32)
+    ours = np.array([contract(float(v)) for v in x], dtype=np.float32)
+    theirs = cuda_fn(torch.from_numpy(x.copy()).to(cuda_device)).cpu().numpy()
+    # all values of one sign, so the ulp distance is the distance of the bit patterns
+    assert np.all(np.isfinite(ours)) and np.all(ours >= 0) and np.all(theirs >= 0)
+    ulps = np.abs(ours.view(np.int32).astype(np.int64) - theirs.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 3, (which, int(ulps.max()), float(x[ulps.argmax()]))
