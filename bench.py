@@ -215,6 +215,14 @@ def diff_stats(d):
             "p90": float(np.percentile(d, 90)), "p99": float(np.percentile(d, 99))}
 
 
+def host_threads() -> int:
+    """Host cores this process may run on (the oracle's BLAS and OpenMP threads use them)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return 0
@@ -249,7 +257,7 @@ def reference_arm(args, rank, world):
         times.append(s)
     total = sum(times)
     value = args.steps * rows_per_step / total
-    cores = os.cpu_count()
+    cores = host_threads()
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
@@ -492,7 +500,7 @@ def grpo_arm(args, rank, world, dev, dist, W, binding, WL):
         W_bits = WL.bf16_tensor_bits(W)
         hid_bits = WL.bf16_tensor_bits(g.hidden[torch.from_numpy(rows).to(dev)])
         s_, n_ = cpu_oracle_sample(hid_bits, W_bits, g.targets.cpu().numpy()[rows], None)
-        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
                "sample": "%d active rows of the batch over the full vocabulary (%.1f s)" % (n_, s_)}
     if rank == 0:
         ms_per_step = ms_total / K
@@ -938,7 +946,7 @@ def main():
         hid_bits = WL.bf16_tensor_bits(hidden[rows_t])
         s_, n_, ref_lp, ref_lse = cpu_oracle_sample(hid_bits, W_bits, targets.cpu().numpy()[rows],
                                                     None, want_values=True)
-        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": n_ / s_, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
                "sample": "%d rows of the batch over the full vocabulary (%.1f s)" % (n_, s_)}
         got_lp = out_lp[rows_t].double().cpu().numpy()
         got_lse = out_lse[rows_t].double().cpu().numpy()
