@@ -220,7 +220,57 @@ def pin_backward_rows_sum_to_zero(O):
     assert np.all(G[np.arange(5), w.targets] * np.linspace(-2, 2, 5) >= 0)
 
 
+def pin_log_softmax_exact(O):
+    """Full log_softmax of small fp64 logit rows against 50-digit Decimal exp and ln.
+
+    Decimal(x) of a double is exact, so each expected value is l_v - ln(sum_u e^(l_u))
+    with only the Decimal rounding at 50 digits; logits spread over +-40 exercise the max
+    shift.  The outputs of an inactive row are 0."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(21)
+    for T, V in ((1, 1), (2, 2), (3, 17), (2, 130)):
+        L = rng.uniform(-40.0, 40.0, size=(T, V))
+        act = np.ones(T, dtype=np.uint8)
+        act[-1] = 0 if T > 1 else 1
+        out = O.log_softmax_from_logits(L, act)
+        for t in range(T):
+            if not act[t]:
+                assert np.all(out[t] == 0.0), (T, V, t)
+                continue
+            ln_sum = sum(Decimal(float(x)).exp() for x in L[t]).ln()
+            for v in range(V):
+                want = float(Decimal(float(L[t, v])) - ln_sum)
+                assert abs(out[t, v] - want) <= 1e-13 * max(1.0, abs(want)), (T, V, t, v)
+
+
+def pin_log_softmax_normalised(O):
+    """Every active row of exp(log_softmax) sums to 1, and a row of equal logits gives -ln V."""
+    rng = np.random.default_rng(22)
+    L = rng.standard_normal((4, 3000)) * 6.0 + 25.0    # max far from 0
+    out = O.log_softmax_from_logits(L)
+    for t in range(4):
+        assert abs(math.fsum(math.exp(x) for x in out[t]) - 1.0) <= 1e-12, t
+    g = _golden("closed_forms.json")["neg_log_V"]
+    for V in (2, 1024, 151936):
+        row = np.full((1, V), 3.75)
+        assert np.all(np.abs(O.log_softmax_from_logits(row) - g[str(V)]) <= 1e-12), V
+
+
+def pin_log_softmax_shift_and_selection(O):
+    """Adding c to a row leaves its log_softmax unchanged, and the entry at a row's target is
+    the selected-token logprob of the pinned (logprob, lse) oracle on the same logits."""
+    rng = np.random.default_rng(23)
+    L = rng.standard_normal((5, 777)) * 4.0
+    base = O.log_softmax_from_logits(L)
+    for c in (-70.5, 3.25, 96.0):
+        assert np.all(np.abs(O.log_softmax_from_logits(L + c) - base) <= 1e-12 * (1 + abs(c))), c
+    tg = rng.integers(0, 777, 5)
+    lp, _ = O.lse_and_logprob_from_logits(L, tg)
+    assert np.all(np.abs(base[np.arange(5), tg] - lp) <= 1e-13 * np.maximum(1.0, np.abs(lp)))
+
+
 ALL_PINS = [pin_bf16_decode, pin_brute_force_tiny, pin_constant_logits, pin_two_class_softplus,
             pin_probabilities_sum_to_one, pin_shift_invariance, pin_shard_merge, pin_tile_tree,
             pin_vocab_permutation, pin_masks_and_bad_targets, pin_backward_finite_differences,
-            pin_backward_rows_sum_to_zero]
+            pin_backward_rows_sum_to_zero, pin_log_softmax_exact, pin_log_softmax_normalised,
+            pin_log_softmax_shift_and_selection]

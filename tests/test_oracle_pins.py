@@ -136,10 +136,44 @@ def _mut_grad_transposed(m):
     m.backward = backward
 
 
+def _patch_log_softmax(m, fn):
+    m.log_softmax_from_logits = fn
+
+
+def _mut_log_softmax_drop_max(m):
+    def f(L, active=None):  # lse without the max it was shifted by
+        M = L.max(axis=1)
+        return L - np.log(np.exp(L - M[:, None]).sum(axis=1))[:, None]
+    _patch_log_softmax(m, f)
+
+
+def _mut_log_softmax_sign(m):
+    def f(L, active=None):
+        M = L.max(axis=1)
+        return (M + np.log(np.exp(L - M[:, None]).sum(axis=1)))[:, None] - L
+    _patch_log_softmax(m, f)
+
+
+def _mut_log_softmax_dropped_column(m):
+    def f(L, active=None):  # the sum misses the last vocabulary column
+        M = L.max(axis=1)
+        out = L - (M + np.log(np.exp(L[:, :-1] - M[:, None]).sum(axis=1)))[:, None]
+        if active is not None:
+            out = np.where(np.asarray(active).astype(bool)[:, None], out, 0.0)
+        return out
+    _patch_log_softmax(m, f)
+
+
+def _mut_log_softmax_mask_ignored(m):
+    orig = m.log_softmax_from_logits
+    m.log_softmax_from_logits = lambda L, active=None: orig(L, None)
+
+
 MUTANTS = [_mut_decode_shift, _mut_k_reversed, _mut_drop_max, _mut_target_off_by_one,
            _mut_wrong_sign, _mut_exp_sign, _mut_dropped_term, _mut_mask_ignored,
            _mut_floor_split, _mut_merge_unweighted, _mut_grad_sign, _mut_grad_unscaled,
-           _mut_grad_transposed]
+           _mut_grad_transposed, _mut_log_softmax_drop_max, _mut_log_softmax_sign,
+           _mut_log_softmax_dropped_column, _mut_log_softmax_mask_ignored]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda f: f.__name__)
