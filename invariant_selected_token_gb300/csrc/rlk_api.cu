@@ -34,7 +34,6 @@ struct DeviceState {
     bool ready = false;
     int sm_count = 0;
     int cc = 0;             // 10 * major + minor
-    int pair_clusters = 0;  // 2-CTA clusters of the logits kernel that fit at once
     int mat_ctas_per_sm[2] = {0, 0};  // materialised-logits kernel, fp32 / bf16
 };
 
@@ -119,8 +118,7 @@ rlk_status_t device_check(DeviceState** out) {
         st.cc = major * 10 + minor;
         st.sm_count = sms;
         if (st.cc == 103) {
-            if (rlk::prepare_tile_partials_kernels(&st.pair_clusters) != cudaSuccess)
-                return RLK_ERR_CUDA;
+            if (rlk::prepare_tile_partials_kernels() != cudaSuccess) return RLK_ERR_CUDA;
             if (rlk::prepare_gemm_kernels() != cudaSuccess) return RLK_ERR_CUDA;
             if (rlk::prepare_mat_kernels(st.mat_ctas_per_sm) != cudaSuccess) return RLK_ERR_CUDA;
             if (rlk::prepare_tree_kernels() != cudaSuccess) return RLK_ERR_CUDA;
@@ -157,19 +155,6 @@ rlk_status_t encode_bf16_map(CUtensorMap* map, const void* base, int64_t inner, 
     return r == CUDA_SUCCESS ? RLK_OK : RLK_ERR_CUDA;
 }
 
-// Paired (2-CTA cluster, W tile multicast) schedule for batches of more than
-// one token tile.  Both schedules issue the same MMAs per logit, so the
-// choice never changes a bit; RLK_TEST_PAIR=0|1 forces one (tests use it).
-// The pair reads each W tile from L2 once instead of twice; measured on
-// GB300 that saves power more than the pair's lockstep costs once the GPU
-// runs at its power limit (a training step, or a few hundred calls in a
-// row): packed T = 4096 +0.7 % at the same power, a long GRPO batch +3.5 %.
-bool use_pair(int64_t T, const DeviceState* dev) {
-    bool pair = true;
-    if (const char* f = std::getenv("RLK_TEST_PAIR")) pair = std::atoi(f) != 0;
-    return pair && T > kTileM && dev->pair_clusters >= 1;
-}
-
 // RLK_TEST_DROP_STAGE=1 (the logits kernel) or 2 (the grad_hidden GEMM): CTA
 // 0's producer skips its first pipeline stage, so its MMA wait runs out
 // (bounded) and the kernel reports RLK_ERR_TIMEOUT -- the failure-detection
@@ -188,10 +173,9 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     // one token tile: load only the rows that exist (rounded up to a whole
     // 8-row swizzle atom); the MMA's other accumulator rows are discarded
     const int a_rows = T >= kTileM ? kTileM : int((T + 7) / 8 * 8);
-    const bool pair = use_pair(T, dev);
     rlk_status_t s = encode_bf16_map(&map_h, hidden, H, T, uint32_t(a_rows));
     if (s != RLK_OK) return s;
-    s = encode_bf16_map(&map_w, W, H, V_local, pair ? kTileN / 2 : kTileN);
+    s = encode_bf16_map(&map_w, W, H, V_local, kTileN);
     if (s != RLK_OK) return s;
     rlk::TilePartialsArgs a;
     a.targets = targets;
@@ -214,8 +198,7 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     a.V_total = V_local;
     return rlk::launch_tile_partials(map_h, map_w, a,
                                      dbg != nullptr ? rlk::kEpiDebugLogits : rlk::kEpiPartials,
-                                     pair, dev->sm_count, dev->pair_clusters,
-                                     stream) == cudaSuccess
+                                     dev->sm_count, stream) == cudaSuccess
                ? RLK_OK
                : RLK_ERR_CUDA;
 }
@@ -606,9 +589,8 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
     // 1. logits again, then G = g (onehot - softmax) in bf16 (the forward's lse)
     CUtensorMap map_h, map_w;
     const int a_rows = T >= kTileM ? kTileM : int((T + 7) / 8 * 8);
-    const bool pair = use_pair(T, dev);
     if ((s = encode_bf16_map(&map_h, hidden, H, T, uint32_t(a_rows))) != RLK_OK) return s;
-    if ((s = encode_bf16_map(&map_w, W, H, V, pair ? kTileN / 2 : kTileN)) != RLK_OK) return s;
+    if ((s = encode_bf16_map(&map_w, W, H, V, kTileN)) != RLK_OK) return s;
     rlk::TilePartialsArgs a;
     std::memset(&a, 0, sizeof(a));
     a.targets = targets;
@@ -625,8 +607,8 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
     a.G = G;
     a.ldG = ldG;
     a.V_total = V;
-    if (rlk::launch_tile_partials(map_h, map_w, a, rlk::kEpiGrad, pair, dev->sm_count,
-                                  dev->pair_clusters, st) != cudaSuccess)
+    if (rlk::launch_tile_partials(map_h, map_w, a, rlk::kEpiGrad, dev->sm_count, st) !=
+        cudaSuccess)
         return RLK_ERR_CUDA;
 
     // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum.

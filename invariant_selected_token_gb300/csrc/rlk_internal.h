@@ -41,15 +41,12 @@ struct TilePartialsArgs {
 
 enum TileEpilogue { kEpiPartials = 0, kEpiDebugLogits = 1, kEpiGrad = 2 };
 
-// hidden map: bf16 [T][H], box 64 x 128; weight map: bf16 [V_local][H], box 64 x 256.
-// pair: clusters of two CTAs sharing each W tile by multicast (needs T > 128
-// and a W map whose box is 128 rows, half a W tile); pair_clusters: how many
-// such clusters fit on the device at once.
+// hidden map: bf16 [T][H], box 64 x a_box_rows; weight map: bf16 [V_local][H], box 64 x 256.
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                                 const TilePartialsArgs& a, int epilogue, bool pair, int num_sms,
-                                 int pair_clusters, cudaStream_t stream);
+                                 const TilePartialsArgs& a, int epilogue, int num_sms,
+                                 cudaStream_t stream);
 int tile_partials_smem_bytes();
-cudaError_t prepare_tile_partials_kernels(int* pair_clusters);
+cudaError_t prepare_tile_partials_kernels();
 
 struct TileTreeArgs {
     const float2* partials;   // [T][ld]

@@ -106,28 +106,28 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
     }
 }
 
-// Work-unit order.  Units are (W tile n, token unit mu), where a token unit
-// is one token tile (kPair: a pair).  The order is vocabulary-major inside
-// bands of kBandTokenTiles token tiles: every W tile is visited by all of a
-// band's token units before the next W tile, so W is read from HBM once per
-// band while the band's hidden rows (4096 rows = 32 MB at H = 4096) stay in
-// L2.  One band covers T <= 4096; at T = 8192 a single band let the drifting
-// CTAs keep W tiles and 64 MB of hidden rows alive together, and L2 sent
-// 7.9 GB per launch to HBM instead of the 2.6 GB two bands read.
+// Work-unit order.  Units are (W tile n, token tile mu).  The order is
+// vocabulary-major inside bands of kBandTokenTiles token tiles: every W tile
+// is visited by all of a band's token tiles before the next W tile, so W is
+// read from HBM once per band while the band's hidden rows (4096 rows = 32
+// MB at H = 4096) stay in L2.  One band covers T <= 4096; at T = 8192 a
+// single band let the drifting CTAs keep W tiles and 64 MB of hidden rows
+// alive together, and L2 sent 7.9 GB per launch to HBM instead of the 2.6 GB
+// two bands read.
 constexpr int kBandTokenTiles = 32;
 
 struct UnitCoords {
     int n_blk;  // W tile
-    int mu;     // token unit
+    int mu;     // token tile
 };
 
-// unit -> (W tile, token unit) for num_n W tiles, num_mu token units and
-// band_mu token units per band (the last band may hold fewer).
+// unit -> (W tile, token tile) for num_n W tiles, num_mu token tiles and
+// band_mu token tiles per band (the last band may hold fewer).
 __device__ __forceinline__ UnitCoords unit_coords(int unit, int num_n, int num_mu, int band_mu) {
     const int full = band_mu * num_n;  // units of a full band
     const int band = unit / full;
     const int first_mu = band * band_mu;
-    const int mus = min(band_mu, num_mu - first_mu);  // token units of this band
+    const int mus = min(band_mu, num_mu - first_mu);  // token tiles of this band
     const int within = unit - band * full;
     UnitCoords c;
     c.n_blk = within / mus;
@@ -135,13 +135,7 @@ __device__ __forceinline__ UnitCoords unit_coords(int unit, int num_n, int num_m
     return c;
 }
 
-// kPair: CTAs run in clusters of two along the token dimension.  Both CTAs of
-// a cluster work on the same W slice (token tiles 2p and 2p+1): each loads
-// its own hidden tile and one half (128 rows) of the W tile, multicast into
-// both CTAs' shared memory, so each W byte crosses L2 once per pair.  Each
-// CTA still issues its own M=128, N=256 MMAs on the full W tile, so the
-// arithmetic -- and every bit -- is that of the unpaired kernel.
-template <int kEpi, bool kPair>
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
                     const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
@@ -161,19 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int num_m = (a.T + kTileM - 1) / kTileM;
     const int num_n = (a.V_local + kTileN - 1) / kTileN;
-    // a work unit is one W tile and one token tile (kPair: a pair of token tiles)
-    const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
-    const int num_mu = kPair ? (num_m + 1) / 2 : num_m;
-    const int band_mu = kPair ? kBandTokenTiles / 2 : kBandTokenTiles;
-    const int total = num_mu * num_n;
-    const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-    const int ustride = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    // a work unit is one W tile and one token tile
+    const int total = num_m * num_n;
+    const int unit0 = static_cast<int>(blockIdx.x);
+    const int ustride = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            // kPair: a stage is free once both CTAs' MMAs have read it
-            ptx::mbar_init(&empty[s], kPair ? 2 : 1);
+            ptx::mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -190,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before_sync();
     __syncthreads();
-    if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any multicast
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     // With programmatic dependent launch the set-up above overlaps the
@@ -209,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage = 1;
             }
             for (int unit = unit0; unit < total && !*abort_flag; unit += ustride) {
-                const UnitCoords uc = unit_coords(unit, num_n, num_mu, band_mu);
+                const UnitCoords uc = unit_coords(unit, num_n, num_m, kBandTokenTiles);
                 const int n_blk = uc.n_blk;
-                const int m_blk = kPair ? 2 * uc.mu + static_cast<int>(rank) : uc.mu;
+                const int m_blk = uc.mu;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
                         *abort_flag = 1;
@@ -221,16 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(&full[stage], a_bytes + kStageBytesB);
                     ptx::tma_load_2d(sA + stage * kStageBytesA, &map_hidden, &full[stage],
                                      kb * kBlockK, m_blk * kTileM);
-                    if (kPair) {
-                        // this CTA's half of the W tile, into both CTAs
-                        ptx::tma_load_2d_multicast(sB + stage * kStageBytesB + rank * (kStageBytesB / 2),
-                                                   &map_w, &full[stage], kb * kBlockK,
-                                                   n_blk * kTileN + static_cast<int>(rank) * (kTileN / 2),
-                                                   static_cast<uint16_t>(0x3));
-                    } else {
-                        ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
-                                         kb * kBlockK, n_blk * kTileN);
-                    }
+                    ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
+                                     kb * kBlockK, n_blk * kTileN);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -266,10 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       ptx::smem_desc_k_sw128(b0 + kk * 32), kIdesc,
                                       (kb | kk) != 0 ? 1u : 0u);
                     }
-                    if (kPair)
-                        ptx::mma_commit_multicast(&empty[stage], static_cast<uint16_t>(0x3));
-                    else
-                        ptx::mma_commit(&empty[stage]);
+                    ptx::mma_commit(&empty[stage]);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -293,9 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         for (int unit = unit0; unit < total; unit += ustride) {
-            const UnitCoords uc = unit_coords(unit, num_n, num_mu, band_mu);
+            const UnitCoords uc = unit_coords(unit, num_n, num_m, kBandTokenTiles);
             const int n_blk = uc.n_blk;
-            const int m_blk = kPair ? 2 * uc.mu + static_cast<int>(rank) : uc.mu;
+            const int m_blk = uc.mu;
             // last unit of this CTA: let the next kernel (the tile tree) start
             // launching; it waits for this grid before reading anything
             if (unit + ustride >= total) ptx::grid_dependents_launch();
@@ -375,9 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     __syncthreads();
-    // kPair: neither CTA leaves while the other may still multicast into it
-    // or arrive on its barriers
-    if (kPair) ptx::cluster_sync();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
@@ -387,91 +362,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int kEpi>
 cudaError_t set_smem_attr() {
-    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<kEpi, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_tile_partials<kEpi, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-}
-
-// Clusters of two CTAs that fit at once on this device (0 if none).
-int max_pair_clusters() {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_tile_partials<kEpiPartials, true>, &cfg) != cudaSuccess)
-        return 0;
-    return n;
+    return cudaFuncSetAttribute(k_tile_partials<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemBytes);
 }
 
 template <int kEpi>
 cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                       const TilePartialsArgs& a, bool pair, int num_sms, int pair_clusters,
-                       cudaStream_t stream) {
+                       const TilePartialsArgs& a, int num_sms, cudaStream_t stream) {
     const int num_m = (a.T + kTileM - 1) / kTileM;
     const int num_n = (a.V_local + kTileN - 1) / kTileN;
-    if (!pair) {
-        const int64_t total = static_cast<int64_t>(num_m) * num_n;
-        const int grid = static_cast<int>(total < num_sms ? total : num_sms);
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, false>, map_hidden, map_w, a);
-    }
-    const int64_t units = static_cast<int64_t>((num_m + 1) / 2) * num_n;
-    const int clusters = static_cast<int>(units < pair_clusters ? units : pair_clusters);
+    const int64_t total = static_cast<int64_t>(num_m) * num_n;
+    const int grid = static_cast<int>(total < num_sms ? total : num_sms);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, true>, map_hidden, map_w, a);
+    return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi>, map_hidden, map_w, a);
 }
 
 }  // namespace
 
 int tile_partials_smem_bytes() { return kSmemBytes; }
 
-cudaError_t prepare_tile_partials_kernels(int* pair_clusters) {
+cudaError_t prepare_tile_partials_kernels() {
     cudaError_t e;
     if ((e = set_smem_attr<kEpiPartials>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<kEpiDebugLogits>()) != cudaSuccess) return e;
-    if ((e = set_smem_attr<kEpiGrad>()) != cudaSuccess) return e;
-    *pair_clusters = max_pair_clusters();
-    return cudaSuccess;
+    return set_smem_attr<kEpiGrad>();
 }
 
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
-                                 const TilePartialsArgs& a, int epilogue, bool pair, int num_sms,
-                                 int pair_clusters, cudaStream_t stream) {
+                                 const TilePartialsArgs& a, int epilogue, int num_sms,
+                                 cudaStream_t stream) {
     if (epilogue == kEpiDebugLogits)
-        return launch_epi<kEpiDebugLogits>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
-    if (epilogue == kEpiGrad)
-        return launch_epi<kEpiGrad>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
-    return launch_epi<kEpiPartials>(map_hidden, map_w, a, pair, num_sms, pair_clusters, stream);
+        return launch_epi<kEpiDebugLogits>(map_hidden, map_w, a, num_sms, stream);
+    if (epilogue == kEpiGrad) return launch_epi<kEpiGrad>(map_hidden, map_w, a, num_sms, stream);
+    return launch_epi<kEpiPartials>(map_hidden, map_w, a, num_sms, stream);
 }
 
 }  // namespace rlk

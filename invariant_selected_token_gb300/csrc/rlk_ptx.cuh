@@ -92,20 +92,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-// Same as tma_load_2d, but the box lands at the same shared-memory offset in
-// every CTA of `cta_mask` (this cluster), each completing bytes on its own
-// barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map,
-                                                      uint64_t* bar, int32_t c0, int32_t c1,
-                                                      uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- dependent launch
 // Wait until the grids this one depends on (launched before it in the stream)
 // have completed and their memory is visible; a no-op without programmatic
@@ -118,20 +104,6 @@ __device__ __forceinline__ void grid_dependency_wait() {
 // this one at its own grid_dependency_wait before touching shared data).
 __device__ __forceinline__ void grid_dependents_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Whole-cluster barrier (every thread of every CTA in the cluster).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -179,16 +151,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_addr(bar))
-        : "memory");
-}
-
-// Like mma_commit, but the arrival lands on the barrier at the same offset in
-// every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(cta_mask)
         : "memory");
 }
 

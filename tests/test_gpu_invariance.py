@@ -158,22 +158,6 @@ def test_tree_layouts_agree(rlk, cuda_device, monkeypatch, T, H, V):
         assert torch.equal(a_part, b_part), "shard record n=%d" % n
 
 
-@pytest.mark.parametrize("T,H,V", [(129, 128, 1000), (300, 256, 5000), (1024, 512, 30000)])
-def test_paired_and_single_cta_schedules_agree(rlk, cuda_device, monkeypatch, T, H, V):
-    """W-tile multicast across CTA pairs only moves data: same MMAs, same bits (and grads)."""
-    w = WL.to_device(WL.small_case(T, H, V, seed=T + 17, w_std=0.05, inactive_frac=0.1), cuda_device)
-    g = torch.randn(T, generator=torch.Generator(device=cuda_device).manual_seed(3), device=cuda_device)
-    outs = []
-    for pair in ("0", "1"):
-        monkeypatch.setenv("RLK_TEST_PAIR", pair)
-        lp, lse = rlk.linear_logprob(w.hidden, w.W, w.targets, w.active, 2)
-        dh, dW = rlk.linear_logprob_backward(w.hidden, w.W, w.targets, g, lse, w.active)
-        outs.append((lp, lse, dh, dW))
-    monkeypatch.delenv("RLK_TEST_PAIR")
-    for a, b, name in zip(outs[0], outs[1], ("logprob", "lse", "grad_hidden", "grad_W")):
-        assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
-
-
 @pytest.mark.parametrize("T,H,V", [(1, 256, 5000), (300, 512, 20000)])
 def test_inputs_written_just_before_each_call(rlk, cuda_device, T, H, V):
     """The logits and tile-tree kernels start early (programmatic dependent launch) and

@@ -132,19 +132,17 @@ def test_qwen_logit_accuracy(rlk, qwen):
     assert np.abs(err).max() <= 2e-5 * (1 + np.abs(ref).max()), stats
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
-def test_token_tile_bands_ragged(rlk, cuda_device, monkeypatch, pair):
+def test_token_tile_bands_ragged(rlk, cuda_device):
     """T = 8322: 66 token tiles (the last one 2 rows), i.e. three bands of 32 tiles for the
-    logits kernel's work order, the last band holding a single (pair of) tile(s).  Every
-    row against the oracle, and bit for bit against the same rows computed in batches of
-    4096 and of 130 rows (one band, different band boundaries)."""
-    monkeypatch.setenv("RLK_TEST_PAIR", pair)
+    logits kernel's work order, the last band holding two tiles.  Every row against the
+    oracle, and bit for bit against the same rows computed in batches of 4096 and of 130
+    rows (one band, different band boundaries)."""
     T, H, V = 8322, 128, 3000
     w = WL.small_case(T, H, V, seed=77, n_shards=2)
     dw = WL.to_device(w, cuda_device)
     lp, lse = run(rlk, dw, 2)
     ref_lp, ref_lse = O.selected_logprob(w.hidden, w.W, w.targets)
-    assert_close(lp, lse, ref_lp, ref_lse, "T=8322 pair=%s" % pair)
+    assert_close(lp, lse, ref_lp, ref_lse, "T=8322")
     for bsz in (4096, 130):
         for b0 in range(0, T, bsz):
             b1 = min(T, b0 + bsz)

@@ -1,7 +1,7 @@
 """The logits kernel's and the backward GEMM's work orders, replayed on the CPU.
 
 ``unit_coords`` in ``csrc/rlk_logits.cu`` maps a work unit to (W tile, token
-unit) in bands of 32 token tiles, vocabulary-major inside a band; the GEMM's
+tile) in bands of 32 token tiles, vocabulary-major inside a band; the GEMM's
 ``decode`` in ``csrc/rlk_gemm.cu`` takes N tiles in bands when ``n_band`` is
 set.  Each must visit every tile exactly once (a skipped or repeated tile
 would leave logits unreduced or reduce them twice), and the bands must come
@@ -34,12 +34,11 @@ def gemm_decode(r, num_m, num_n, n_band):
     return m_blk, first_n + (within - m_blk * nb)
 
 
-@pytest.mark.parametrize("pair", [False, True])
-def test_logits_units_cover_every_tile_once_band_by_band(pair):
-    band_mu = 16 if pair else 32
+def test_logits_units_cover_every_tile_once_band_by_band():
+    band_mu = 32
     for num_n in (1, 2, 3, 7, 594):
         for num_m in list(range(1, 70)) + [127, 128, 129]:
-            num_mu = (num_m + 1) // 2 if pair else num_m
+            num_mu = num_m
             seq = [unit_coords(u, num_n, num_mu, band_mu) for u in range(num_mu * num_n)]
             assert sorted(seq) == [(n, m) for n in range(num_n) for m in range(num_mu)]
             bands = [m // band_mu for _, m in seq]
