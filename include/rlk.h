@@ -338,12 +338,20 @@ rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma,
  *     RLK_STATIC_WS_BYTES are refused with RLK_ERR_WORKSPACE; at V = 151936
  *     that is about 1700 tokens per call with 4 shards.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current).  Under CUDA's
+ *     default lazy module loading that lookup also loads the array itself,
+ *     so the first call on a device is the one that still needs 16 MiB of
+ *     free device memory: make it at start-up, before reserving the rest of
+ *     the memory (a KV cache), and before any stream capture.  Later calls
+ *     need no free memory at all.
+ *   - The looked-up address belongs to the device's primary context: do not
+ *     reset the device (cudaDeviceReset) or call from another context
+ *     between calls.
  *   - All calls on a device share the array: calls that overlap on the GPU
  *     (e.g. on two unordered streams) race; order them.  Nothing in the
  *     array needs to start at zero.
- * Other arguments and errors as rlk_linear_logprob.
+ * Other arguments and errors (and the order in which they are checked) as
+ * rlk_linear_logprob; RLK_ERR_CUDA also if the address lookup fails.
  */
 #define RLK_STATIC_WS_BYTES (16u << 20)
 rlk_status_t rlk_linear_logprob_static_ws(const void* hidden, const void* W,

@@ -15,7 +15,13 @@
 // array's name as a device address (on the host it names a stand-in
 // object), so the device address is fetched once per device with
 // cudaGetSymbolAddress, with that device current, on the first call made
-// on that device; make that first call before any stream capture.
+// on that device.  Under CUDA's default lazy module loading that lookup is
+// also what loads this file's module and with it the array's 16 MiB, so the
+// first call on each device is the one that can still fail for lack of
+// memory: make it at start-up, before the caller reserves the rest of the
+// device's memory (a KV cache), and before any stream capture.  The cached
+// address belongs to the device's primary context: do not reset the device
+// (cudaDeviceReset) or switch to another context between calls.
 //
 // Sharing.  All calls on one device use the same array, and it keeps
 // whatever the previous call left in it.  Nothing in it has to start at
@@ -24,10 +30,10 @@
 // issued on two streams without ordering between them) race on the array;
 // order them on one stream or synchronise between them.
 //
-// Everything else -- the kernels, the arithmetic, the bits -- is that of
-// rlk_linear_logprob: this call runs the same two stages, rlk_tile_partials
-// and rlk_tile_merge, on the built-in array.  It calls no cudaMalloc,
-// cudaFree or other allocating routine.
+// Everything else -- the argument checks, the kernels, the arithmetic, the
+// bits -- is that of rlk_linear_logprob: this call is rlk_linear_logprob on
+// the built-in array.  It calls no cudaMalloc, cudaFree or other allocating
+// routine.
 #include <cstdint>
 #include <mutex>
 
@@ -65,22 +71,12 @@ extern "C" rlk_status_t rlk_linear_logprob_static_ws(
     const void* hidden, const void* W, const int32_t* targets, const uint8_t* active_mask,
     int64_t T, int64_t H, int64_t V, int n_shards, float* out_logprob, float* out_lse,
     int32_t* dev_status, rlk_stream_t stream) {
-    if (T == 0) return RLK_OK;
-    if (T < 0 || T > RLK_MAX_ROWS) return RLK_ERR_INVALID_ARG;
-    const size_t need = rlk_workspace_size(T, V, n_shards);
-    if (need == 0) {
-        // invalid V / n_shards: let the stage report the precise code
-        return rlk_tile_partials(hidden, W, targets, active_mask, T, H, V, n_shards, nullptr, 0,
-                                 dev_status, stream);
-    }
-    if (need > RLK_STATIC_WS_BYTES) return RLK_ERR_WORKSPACE;
-    if (!out_logprob || !out_lse) return RLK_ERR_INVALID_ARG;
     void* ws = nullptr;
-    rlk_status_t s = static_ws_address(&ws);
+    const rlk_status_t s = static_ws_address(&ws);
     if (s != RLK_OK) return s;
-    s = rlk_tile_partials(hidden, W, targets, active_mask, T, H, V, n_shards, ws,
-                          RLK_STATIC_WS_BYTES, dev_status, stream);
-    if (s != RLK_OK) return s;
-    return rlk_tile_merge(targets, active_mask, T, V, n_shards, out_logprob, out_lse, ws,
-                          RLK_STATIC_WS_BYTES, dev_status, stream);
+    // rlk_linear_logprob checks every argument in its own order and refuses a
+    // batch whose workspace exceeds the array with RLK_ERR_WORKSPACE before
+    // anything is launched, so both calls report the same codes.
+    return rlk_linear_logprob(hidden, W, targets, active_mask, T, H, V, n_shards, out_logprob,
+                              out_lse, ws, RLK_STATIC_WS_BYTES, dev_status, stream);
 }

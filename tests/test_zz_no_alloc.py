@@ -92,3 +92,29 @@ def test_static_scratch_refuses_batches_beyond_its_size(rlk, cuda_device):
     stream = ctypes.c_void_p(torch.cuda.current_stream(cuda_device).cuda_stream)
     rc = fn(_p(h), _p(W), _p(tg), None, T_ok + 1, 64, V, n, _p(out), _p(out), None, stream)
     assert rc == 4  # RLK_ERR_WORKSPACE, nothing launched
+    # a missing output is reported first, as rlk_linear_logprob reports it
+    rc = fn(_p(h), _p(W), _p(tg), None, T_ok + 1, 64, V, n, None, _p(out), None, stream)
+    assert rc == 1  # RLK_ERR_INVALID_ARG
+
+
+def test_static_scratch_later_calls_take_no_device_memory(rlk, cuda_device):
+    """After the first call on the device has loaded the scratch array, further calls leave
+    the device's free memory exactly as it was: nothing is allocated per call."""
+    fn = _static_ws_fn(rlk.lib())
+    status = rlk.new_status(cuda_device)
+    dw = WL.to_device(WL.small_case(200, 256, 7000, seed=43, n_shards=2), cuda_device)
+    rc, _, _ = _call_static(fn, dw, 2, status)   # first call: loads the array if not yet loaded
+    assert rc == 0
+    lp = torch.empty(200, dtype=torch.float32, device=cuda_device)
+    lse = torch.empty_like(lp)
+    stream = ctypes.c_void_p(torch.cuda.current_stream(cuda_device).cuda_stream)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(cuda_device)
+    for _ in range(3):
+        rc = fn(_p(dw.hidden), _p(dw.W), _p(dw.targets), _p(dw.active), 200, 256, 7000, 2,
+                _p(lp), _p(lse), _p(status), stream)
+        assert rc == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(cuda_device)
+    rlk.raise_on_device_status(status)
+    assert free1 == free0, (free0, free1)
