@@ -183,6 +183,82 @@ def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, ms_total: f
     return world * tokens_per_rank * steps / (ms_total / 1000.0)
 
 
+def timed_steps(step, K, stream):
+    """Run K steps between two events on `stream`; every second step (the odd ones; the
+    only one if K = 1) also records events around its logits-kernel launch.  Returns (total ms of the K steps,
+    mean ms of the instrumented kernel launches, how many were instrumented)."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(max(1, K // 2))]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        if k % 2 or K == 1:
+            step(*ev[k // 2])
+        else:
+            step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    return total, statistics.mean(a.elapsed_time(b) for a, b in ev), len(ev)
+
+
+DECODE_SIZES = (1, 64)
+DECODE_STEPS = 200
+
+
+def decode_record(n, W, hidden, targets, out_lp, out_lse, binding, WL, dev, stream, status,
+                  peaks):
+    """One decode batch of n rows of the packed batch (the rollout side's call), timed as
+    the packed steps are: step rate over DECODE_STEPS steps, logits-kernel time from the
+    instrumented half of them, against the HBM roofline (W + the n hidden rows read once).
+    Its outputs must equal the packed run's outputs for the same rows bit for bit."""
+    import torch
+    idx = torch.from_numpy(WL.decode_rows(n)).to(dev)
+    h, tg = hidden[idx].contiguous(), targets[idx].contiguous()
+    ws = binding.new_workspace(n, V, N_SHARDS, dev)
+    lp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def step(ev0=None, ev1=None):
+        if ev0 is not None:
+            ev0.record(stream)
+        binding.tile_partials(h, W, tg, None, N_SHARDS, ws, status, stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        binding.tile_merge(tg, None, V, N_SHARDS, lp, lse, ws, status, stream)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    ms_total, k_ms, n_k = timed_steps(step, DECODE_STEPS, stream)
+    binding.raise_on_device_status(status)
+    step_ms = ms_total / DECODE_STEPS
+    check_kernel_within_step(k_ms, step_ms)
+    nbytes = float(W.numel() * 2 + h.numel() * 2)
+    mism = sum(int((a.view(torch.int32) != b.view(torch.int32)).sum().item())
+               for a, b in ((lp, out_lp[idx]), (lse, out_lse[idx])))
+    maxd = max(float((a.double() - b.double()).abs().max().item())
+               for a, b in ((lp, out_lp[idx]), (lse, out_lse[idx])))
+    achieved = nbytes / (k_ms / 1000.0) / 1e9
+    return {"T": n, "steps": DECODE_STEPS, "ms_per_step": round(step_ms, 5),
+            "tokens_per_s": n / (step_ms / 1000.0), "kernel_ms": round(k_ms, 5),
+            "kernel_launches_timed": n_k, "gpu_launches": 2 * DECODE_STEPS, "bound": "hbm",
+            "bytes": nbytes,
+            "achieved_gbs": round(achieved, 1), "peak_gbs": peaks["hbm_gbs"],
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "step_frac": round(nbytes / (step_ms / 1000.0) / 1e9 / peaks["hbm_gbs"], 4),
+            "invariance_vs_packed": {"mismatch_count": mism, "max_abs_diff": maxd}}
+
+
+def check_kernel_within_step(kernel_ms, step_ms):
+    """The logits kernel is one part of a step: its time cannot exceed the step's.  A
+    violation means the two were not measured on the same work, so refuse the line."""
+    if kernel_ms > step_ms:
+        raise SystemExit("bench: logits kernel %.4f ms > step %.4f ms -- inconsistent timing"
+                         % (kernel_ms, step_ms))
+
+
 def cpu_oracle_sample(hidden_bits, W_bits, targets, rows, want_values=False):
     """Time the fp64 oracle on the listed rows; returns (seconds, rows) and, with
     want_values, also its (logprob, lse) for those rows."""
@@ -794,17 +870,15 @@ def main():
     torch.cuda.synchronize()
     binding.raise_on_device_status(status)
 
-    # ---------------- timed regions (device-resident inputs)
-    # (1) K steps bracketed by two events: the step rate (`value`).  No event sits
-    # between the two kernels here: an event recorded there would stop the tile
-    # tree from launching early behind the logits kernel (programmatic dependent
-    # launch), which costs a decode step ~7 us.
-    # (2) the same K steps with events around every logits-kernel launch: its
-    # average launch duration, for the roofline.
+    # ---------------- timed region (device-resident inputs)
+    # K steps bracketed by two events give the step rate (`value`).  Inside the same
+    # region, every second step also records events around its logits-kernel launch:
+    # their average is the kernel's duration for the roofline.  Both numbers come from
+    # one pass at one clock, and each timed kernel lies inside the region, so the
+    # kernel time cannot exceed the step time.  (An event between the two kernels keeps
+    # the tile tree from launching early behind the logits kernel -- programmatic
+    # dependent launch -- which costs the instrumented steps a few microseconds.)
     K = args.steps
-    k1_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if dist is not None:
         dist.barrier()
@@ -812,21 +886,11 @@ def main():
     clocks.start()
     time.sleep(0.3)
     t_host0 = time.time()
-    start.record(stream)
-    for k in range(K):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    ms_total = start.elapsed_time(end)
-    for k in range(K):
-        step(*k1_ev[k])
-    torch.cuda.synchronize()
+    ms_total, k1_ms, n_k1 = timed_steps(step, K, stream)
     t_host1 = time.time()
     clk = clocks.stop(t_host0, t_host1)
-    k1_ms = statistics.mean(a.elapsed_time(b) for a, b in k1_ev)
     binding.raise_on_device_status(status)
+    check_kernel_within_step(k1_ms, ms_total / K)
     ms_total = max_over_ranks(ms_total, dist, dev)
     ms_per_step = ms_total / K
     value = weak_scaling_value(world, T, K, ms_total)
@@ -914,8 +978,8 @@ def main():
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "traffic": traffic, "peak_kind": "copy bandwidth (%s)" % peaks["source"]}
     roofline.update({"kernel": "k_tile_partials", "kernel_ms": round(k1_ms, 4),
-                     "kernel_timing": "a second pass of the same K steps with CUDA events "
-                                      "around every launch of the kernel",
+                     "kernel_timing": "CUDA events around the kernel's launch in every second "
+                                      "step of the timed region (%d launches)" % n_k1,
                      "algorithmic": {"flops": flops, "bytes": nbytes}})
     step_roof_ms = max(t_tensor, t_hbm) * 1000.0
 
@@ -936,6 +1000,15 @@ def main():
     mism = sum(int((a.view(torch.int32) != b.view(torch.int32)).sum().item()) for a, b in pairs)
     maxd = max(float((a.double() - b.double()).abs().max().item()) for a, b in pairs)
     invariance = {"mismatch_count": mism, "max_abs_diff": maxd, "compared": layouts}
+
+    # ---------------- decode batches of the packed run's rows (rollout side), timed the
+    # same way, bit-compared with the packed run's outputs for those rows
+    decode = None
+    if args.workload == "packed":
+        decode = {}
+        for n in DECODE_SIZES:
+            decode["T%d" % n] = decode_record(n, W, hidden, targets, out_lp, out_lse, binding, WL,
+                                              dev, stream, status, load_peaks())
 
     # ---------------- CPU baseline: the fp64 oracle on a bounded sample (rank 0, N=1),
     # whose values also give the parity of the timed run's outputs on those rows
@@ -970,6 +1043,7 @@ def main():
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                "gpu_launches": 2 * K, "clocks": clk,
                "active_tokens_per_step": T, "invariance": invariance, "parity": parity,
+               "decode": decode,
                "peak_memory_gb": round(torch.cuda.max_memory_allocated(dev) / 1e9, 3),
                "hardware": hardware_fingerprint(dev),
                "contract": binding.contract_id(), "build": binding.build_fingerprint()}
