@@ -94,6 +94,22 @@ def test_qwen_packed_sampled_rows(rlk, qwen):
     assert 10.0 < np.median(ref_lse) < 16.0
 
 
+@pytest.mark.parametrize("n", [1, 64])
+def test_qwen_decode_rows_against_oracle(rlk, qwen, n):
+    """Decode batches as the rollout side issues them (T = 1 and T = 64 rows of the packed
+    batch, the single-token-tile schedule with a shrunk hidden box), every row against the
+    oracle directly -- not only through their bitwise equality with the packed rows."""
+    pk = qwen.packed
+    rows = WL.decode_rows(n)
+    idx = torch.from_numpy(rows).to(qwen.device)
+    dw = WL.DeviceWorkload("decode%d" % n, pk.hidden[idx].contiguous(), qwen.W,
+                           pk.targets[idx].contiguous())
+    lp, lse = run(rlk, dw, 4)
+    ref_lp, ref_lse = O.selected_logprob(WL.bf16_tensor_bits(dw.hidden), qwen.W_bits,
+                                         dw.targets.cpu().numpy())
+    assert_close(lp, lse, ref_lp, ref_lse, "qwen decode T=%d" % n)
+
+
 @pytest.mark.slow
 def test_qwen_grpo_long_sampled(rlk, qwen):
     """Long-response GRPO batch (~221k rows, prompt rows masked) in 8192-row calls; a seeded
