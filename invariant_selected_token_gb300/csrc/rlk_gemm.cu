@@ -33,7 +33,13 @@ constexpr uint32_t kBytesA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBytesB = kBN * kBK * 2;  // 32 KB
 constexpr uint32_t kAtomBytes = 64 * kBK * 2;  // one MN-major box: 64 MN x 64 K = 8 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * (kBytesA + kBytesB) + 1024 + 256;
+// Epilogue staging: each epilogue warp turns its 32 rows x 32 columns of fp32
+// results around in shared memory (row pitch 36 floats: the eight rows a
+// 16-byte access phase touches fall in distinct bank quads), so that every
+// global store instruction writes whole 128-byte row segments.
+constexpr int kTrPitch = 36;
+constexpr uint32_t kTrBytes = 4 * 32 * kTrPitch * 4;  // four epilogue warps, 18 KB
+constexpr int kSmemBytes = kStages * (kBytesA + kBytesB) + 1024 + 256 + kTrBytes;
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
     if (status) atomicOr(status, 1 << code);
@@ -66,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* transpose = reinterpret_cast<float*>(sB + kStages * kBytesB + 256);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -221,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
+        float* tr = transpose + quad * (32 * kTrPitch);  // this warp's 32 x 32 staging tile
         uint32_t acc = 0, acc_phase = 0;
         for (int unit = blockIdx.x; unit < total; unit += gridDim.x) {
             int split, n_blk, m_blk;
@@ -233,10 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             const int m = m_blk * kBM + row;
             const int n0 = n_blk * kBN;
-            float* dst = g.out + static_cast<int64_t>(split) * g.split_stride +
-                         static_cast<int64_t>(m) * g.ld_out + n0;
+            float* out_split = g.out + static_cast<int64_t>(split) * g.split_stride;
+            float* dst = out_split + static_cast<int64_t>(m) * g.ld_out + n0;
             const bool row_ok = m < g.M;
             const bool vec = g.vec_store && n0 + kBN <= g.N;
+            // staged stores: in pass i, lanes 8j..8j+7 write row 4i + j of the warp's 32
+            // rows, 4 consecutive columns each (one 128-byte segment per row)
+            const int st_row = lane >> 3;
+            const int st_col = (lane & 7) * 4;
 #pragma unroll 1
             for (int q = 0; q < kBN / 32; ++q) {
                 float v[32];
@@ -244,17 +256,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tmem_load_32cols(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                           acc * kBN + q * 32,
                                       v);
-                if (row_ok) {
-                    if (vec) {
+                if (vec) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + q * 32 + i) =
-                                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-                    } else {
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(tr + lane * kTrPitch + i) =
+                            make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    __syncwarp();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + q * 32 + i < g.N) dst[q * 32 + i] = v[i];
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = 4 * i + st_row;
+                        const int mr = m_blk * kBM + quad * 32 + r;
+                        const float4 x = *reinterpret_cast<const float4*>(tr + r * kTrPitch + st_col);
+                        if (mr < g.M)
+                            *reinterpret_cast<float4*>(out_split + static_cast<int64_t>(mr) * g.ld_out +
+                                                       n0 + q * 32 + st_col) = x;
                     }
+                } else if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (n0 + q * 32 + i < g.N) dst[q * 32 + i] = v[i];
                 }
             }
             ptx::tc_fence_before_sync();

@@ -42,6 +42,17 @@ constexpr uint32_t kTmemCols = 512;                      // two 256-column accum
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kTileN);
 constexpr int kSmemBytes = kStages * (kStageBytesA + kStageBytesB) + 1024 /*alignment slack*/
                            + 256 /*barriers, TMEM address, abort flag*/;
+// The backward epilogue turns each warp's 32 rows x 64 columns of bf16 G
+// around in shared memory before storing them, so that every store
+// instruction writes whole 128-byte row segments.  Row pitch 72 elements
+// (144 bytes, an odd number of 16-byte chunks): the eight rows one 16-byte
+// access phase touches fall in distinct bank quads.
+constexpr int kGradPitch = 72;
+constexpr uint32_t kGradStageBytes = 4 * 32 * kGradPitch * 2;  // 18 KB
+template <int kEpi>
+constexpr int smem_bytes_of() {
+    return kSmemBytes + (kEpi == kEpiGrad ? static_cast<int>(kGradStageBytes) : 0);
+}
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
     if (status) atomicOr(status, 1 << code);
@@ -70,9 +81,15 @@ __device__ __forceinline__ MaxSum reduce_tile(float (&v)[kVocabTile], int ncols)
 // Backward epilogue: G[t, c] = bf16_RN(RN(g_t * d)) with d = RN(1 - p) at the
 // target and -p elsewhere, p = rlk_exp(RN(l - lse_t)) -- the gradient of
 // g_t * logprob_t with respect to the logits, from the same fp32 logits and
-// the same exp the forward used.  Inactive rows write zeros.
+// the same exp the forward used.  Inactive rows write zeros; rows at or
+// beyond T write nothing.  Called by the whole warp (lane = row0 + lane's
+// row): each full 64-column half of the tile goes through the warp's staging
+// rows `stage` and out in 128-byte row segments; a ragged last half is
+// stored element by element.
 __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const TilePartialsArgs& a,
-                                          int t, int c0, int ncols, bool valid, int64_t tl) {
+                                          int t, int c0, int ncols, bool valid, int64_t tl,
+                                          uint16_t* stage, int lane, int row0) {
+    const bool row_ok = t < a.T;
     const float lse = valid ? a.lse[t] : 0.0f;
     const float gt = valid ? a.grad[t] : 0.0f;
     const uint64_t neg_lse = f2_splat(-lse);  // RN(l - lse) = RN(l + (-lse))
@@ -80,6 +97,8 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
     uint16_t* dst = a.G + static_cast<int64_t>(t) * a.ldG + c0;
 #pragma unroll
     for (int q = 0; q < kVocabTile / 8; ++q) {
+        const int half = q / 8;
+        const bool staged = half * 64 + 64 <= ncols;  // the same for the whole warp
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -96,12 +115,32 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
             w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
                    (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
         }
-        if (q * 8 + 8 <= ncols) {
-            *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
+        if (staged) {
+            *reinterpret_cast<uint4*>(stage + lane * kGradPitch + (q % 8) * 8) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        } else if (row_ok) {
+            if (q * 8 + 8 <= ncols) {
+                *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (q * 8 + i < ncols) dst[q * 8 + i] = static_cast<uint16_t>(w[i / 2] >> (16 * (i & 1)));
+                for (int i = 0; i < 8; ++i)
+                    if (q * 8 + i < ncols)
+                        dst[q * 8 + i] = static_cast<uint16_t>(w[i / 2] >> (16 * (i & 1)));
+            }
+        }
+        if (staged && q % 8 == 7) {
+            // the half is staged: lanes 8j..8j+7 store row 4i + j, 16 bytes each
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const int ch = lane & 7;
+                const uint4 x = *reinterpret_cast<const uint4*>(stage + r * kGradPitch + ch * 8);
+                if (row0 + r < a.T)
+                    *reinterpret_cast<uint4*>(a.G + static_cast<int64_t>(row0 + r) * a.ldG + c0 +
+                                              half * 64 + ch * 8) = x;
+            }
+            __syncwarp();  // the staging rows are free for the next half
         }
     }
 }
@@ -150,6 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // backward only: per-epilogue-warp staging rows for the G stores
+    uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + kStages * kStageBytesB + 256);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -317,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     }
                     if (kEpi == kEpiGrad) {
-                        if (t < a.T) grad_tile(v, a, t, c0, ncols, valid, tg_local - c0);
+                        grad_tile(v, a, t, c0, ncols, valid, tg_local - c0,
+                                  grad_stage + quad * (32 * kGradPitch), lane,
+                                  m_blk * kTileM + quad * 32);
                         continue;
                     }
                     const int64_t tl = tg_local - c0;
@@ -363,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int kEpi>
 cudaError_t set_smem_attr() {
     return cudaFuncSetAttribute(k_tile_partials<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kSmemBytes);
+                                smem_bytes_of<kEpi>());
 }
 
 template <int kEpi>
@@ -376,7 +419,7 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes_of<kEpi>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
