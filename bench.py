@@ -44,7 +44,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     p.add_argument("--workload", default="packed",
-                   choices=["packed", "decode1", "decode8", "decode64", "decode256",
+                   choices=["packed", "decode1", "decode8", "decode64", "decode128", "decode256",
+                            "decode512",
                             "logits_fp32", "logits_bf16", "log_softmax_fp32", "backward", "grpo",
                             "rmsnorm", "sweep"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
