@@ -185,19 +185,20 @@ def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, ms_total: f
 
 
 def timed_steps(step, K, stream):
-    """Run K steps between two events on `stream`; every second step (the odd ones; the
-    only one if K = 1) also records events around its logits-kernel launch.  Returns (total ms of the K steps,
-    mean ms of the instrumented kernel launches, how many were instrumented)."""
+    """Run K steps between two events on `stream`, each step also recording events around
+    its logits-kernel launch.  Returns (total ms of the K steps, mean ms of the kernel
+    launches, how many were timed).  Every kernel interval lies inside the region and the
+    intervals do not overlap, so the kernel time can never exceed the step time.  (With no
+    event between them, a step's kernels overlap their neighbours' launch and set-up
+    through programmatic dependent launch, and the step can be shorter than one kernel
+    timed alone; the events here cost every step that overlap.)"""
     import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(max(1, K // 2))]
+          for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for k in range(K):
-        if k % 2 or K == 1:
-            step(*ev[k // 2])
-        else:
-            step()
+        step(*ev[k])
     end.record(stream)
     torch.cuda.synchronize()
     total = start.elapsed_time(end)
@@ -211,8 +212,8 @@ DECODE_STEPS = 200
 def decode_record(n, W, hidden, targets, out_lp, out_lse, binding, WL, dev, stream, status,
                   peaks):
     """One decode batch of n rows of the packed batch (the rollout side's call), timed as
-    the packed steps are: step rate over DECODE_STEPS steps, logits-kernel time from the
-    instrumented half of them, against the HBM roofline (W + the n hidden rows read once).
+    the packed steps are: step rate and logits-kernel time over DECODE_STEPS steps,
+    against the HBM roofline (W + the n hidden rows read once).
     Its outputs must equal the packed run's outputs for the same rows bit for bit."""
     import torch
     idx = torch.from_numpy(WL.decode_rows(n)).to(dev)
@@ -873,12 +874,10 @@ def main():
 
     # ---------------- timed region (device-resident inputs)
     # K steps bracketed by two events give the step rate (`value`).  Inside the same
-    # region, every second step also records events around its logits-kernel launch:
-    # their average is the kernel's duration for the roofline.  Both numbers come from
-    # one pass at one clock, and each timed kernel lies inside the region, so the
-    # kernel time cannot exceed the step time.  (An event between the two kernels keeps
-    # the tile tree from launching early behind the logits kernel -- programmatic
-    # dependent launch -- which costs the instrumented steps a few microseconds.)
+    # region every step also records events around its logits-kernel launch: their
+    # average is the kernel's duration for the roofline.  Both numbers come from one
+    # pass at one clock, and the kernel intervals are disjoint parts of the region, so
+    # the kernel time cannot exceed the step time.
     K = args.steps
     clocks = ClockSampler(local)
     if dist is not None:
@@ -979,8 +978,8 @@ def main():
                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                     "traffic": traffic, "peak_kind": "copy bandwidth (%s)" % peaks["source"]}
     roofline.update({"kernel": "k_tile_partials", "kernel_ms": round(k1_ms, 4),
-                     "kernel_timing": "CUDA events around the kernel's launch in every second "
-                                      "step of the timed region (%d launches)" % n_k1,
+                     "kernel_timing": "CUDA events around the kernel's launch in every step of "
+                                      "the timed region (%d launches)" % n_k1,
                      "algorithmic": {"flops": flops, "bytes": nbytes}})
     step_roof_ms = max(t_tensor, t_hbm) * 1000.0
 
