@@ -157,7 +157,8 @@ def _mut_log_softmax_sign(m):
 def _mut_log_softmax_dropped_column(m):
     def f(L, active=None):  # the sum misses the last vocabulary column
         M = L.max(axis=1)
-        out = L - (M + np.log(np.exp(L[:, :-1] - M[:, None]).sum(axis=1)))[:, None]
+        with np.errstate(divide="ignore"):  # a one-column row leaves an empty sum
+            out = L - (M + np.log(np.exp(L[:, :-1] - M[:, None]).sum(axis=1)))[:, None]
         if active is not None:
             out = np.where(np.asarray(active).astype(bool)[:, None], out, 0.0)
         return out
