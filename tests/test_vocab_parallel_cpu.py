@@ -178,3 +178,31 @@ def test_rank_leaving_before_exchange_fails_the_peer_not_hangs():
         p.join(timeout=60)
     assert res[1] == "left before the exchange"
     assert res[0].startswith("error:"), res[0]
+
+
+def _three_main(rank, world, port, out_q):
+    _init(rank, world, port)
+    try:
+        from invariant_selected_token_gb300 import vocab_parallel as VP
+        try:
+            VP.local_vocab_range(1000)
+            out_q.put((rank, "accepted"))
+        except ValueError as e:
+            out_q.put((rank, "refused: %s" % e))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_group_of_three_ranks_is_refused():
+    """The shards are nodes of the tile tree, so a group must have 1, 2, 4 or 8 ranks."""
+    world, port = 3, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_three_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert all(v.startswith("refused") for v in res.values()), res
