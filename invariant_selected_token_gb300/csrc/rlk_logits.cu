@@ -54,6 +54,28 @@ constexpr int smem_bytes_of() {
     return kSmemBytes + (kEpi == kEpiGrad ? static_cast<int>(kGradStageBytes) : 0);
 }
 
+// Ring depth for a hidden box of `a_rows` rows: as many (hidden box, W box)
+// stages as fit in a CTA's shared memory (227 KB) next to the barriers and,
+// for the backward, the G staging rows; at most kMaxStages.  A full 128-row
+// box gives the 4 stages above; the small boxes of decode batches (at most
+// 128 tokens, box rows roundup(T, 8)) give 5 up to 72 rows and 6 up to 40
+// (32 with the G staging): a deeper W stream where the MMAs are nearly
+// free.  Host and device compute it alike.
+constexpr int kMaxStages = 6;
+constexpr int kSmemLimit = 232448;
+__host__ __device__ constexpr int ring_stages(int a_rows, bool grad) {
+    return (kSmemLimit - 1024 - 256 - (grad ? static_cast<int>(kGradStageBytes) : 0)) /
+                       (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB)) > kMaxStages
+               ? kMaxStages
+               : (kSmemLimit - 1024 - 256 - (grad ? static_cast<int>(kGradStageBytes) : 0)) /
+                     (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB));
+}
+template <int kEpi>
+constexpr int ring_smem_bytes(int a_rows) {
+    return ring_stages(a_rows, kEpi == kEpiGrad) * (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB)) +
+           1024 + 256 + (kEpi == kEpiGrad ? static_cast<int>(kGradStageBytes) : 0);
+}
+
 __device__ __forceinline__ void report(int32_t* status, int code) {
     if (status) atomicOr(status, 1 << code);
 }
@@ -174,23 +196,32 @@ __device__ __forceinline__ UnitCoords unit_coords(int unit, int num_n, int num_m
     return c;
 }
 
-template <int kEpi>
+// kFullBox: the hidden box is a full 128-row token tile (batches of more than
+// 128 tokens): the ring is the fixed 4 x 48 KB one.  Otherwise the box holds
+// roundup(T, 8) rows and the ring is sized by ring_stages.
+template <int kEpi, bool kFullBox>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
                     const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    // hidden slots are a_box_rows rows each; the MMA still reads 128 rows from a
+    // slot, and the rows past the box (the next slots' or the W boxes' bytes,
+    // inside this allocation) only feed accumulator rows that are never read
+    const int S = kFullBox ? kStages : ring_stages(a.a_box_rows, kEpi == kEpiGrad);
+    const uint32_t a_stage =
+        kFullBox ? kStageBytesA : static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kStageBytesA;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kStageBytesB);
-    uint64_t* empty = full + kStages;
-    uint64_t* acc_full = empty + kStages;
+    uint8_t* sB = smem + S * a_stage;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * kStageBytesB);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* acc_full = empty + kMaxStages;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // backward only: per-epilogue-warp staging rows for the G stores
-    uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + kStages * kStageBytesB + 256);
+    uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + S * kStageBytesB + 256);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -202,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ustride = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
@@ -249,11 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(&full[stage], a_bytes + kStageBytesB);
-                    ptx::tma_load_2d(sA + stage * kStageBytesA, &map_hidden, &full[stage],
+                    ptx::tma_load_2d(sA + stage * a_stage, &map_hidden, &full[stage],
                                      kb * kBlockK, m_blk * kTileM);
                     ptx::tma_load_2d(sB + stage * kStageBytesB, &map_w, &full[stage],
                                      kb * kBlockK, n_blk * kTileN);
-                    if (++stage == kStages) {
+                    if (++stage == static_cast<uint32_t>(S)) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t a0 = ptx::smem_addr(sA + stage * kStageBytesA);
+                    const uint32_t a0 = ptx::smem_addr(sA + stage * a_stage);
                     const uint32_t b0 = ptx::smem_addr(sB + stage * kStageBytesB);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
@@ -289,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       (kb | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(&empty[stage]);
-                    if (++stage == kStages) {
+                    if (++stage == static_cast<uint32_t>(S)) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -405,8 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int kEpi>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(k_tile_partials<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes_of<kEpi>());
+    const cudaError_t e = cudaFuncSetAttribute(
+        k_tile_partials<kEpi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of<kEpi>());
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_tile_partials<kEpi, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
 }
 
 template <int kEpi>
@@ -419,14 +453,16 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes_of<kEpi>();
+    const bool full_box = a.a_box_rows == kTileM;
+    cfg.dynamicSmemBytes = full_box ? smem_bytes_of<kEpi>() : ring_smem_bytes<kEpi>(a.a_box_rows);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi>, map_hidden, map_w, a);
+    return full_box ? cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, true>, map_hidden, map_w, a)
+                    : cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, false>, map_hidden, map_w, a);
 }
 
 }  // namespace
