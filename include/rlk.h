@@ -179,6 +179,10 @@ rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
  *   out_logprob, out_lse  device, float [T]
  * An active row with no owning shard, or with more than one, gets NaN and
  * sets RLK_ERR_TARGET_RANGE in *dev_status.
+ * The records may come from other processes: with the vocabulary split over
+ * n ranks (rank r holding shard r's W rows and calling
+ * rlk_linear_logprob_shard), gathering every rank's records in rank order and
+ * merging them here on each rank gives every rank the unsharded call's bits.
  */
 rlk_status_t rlk_lse_merge(const rlk_partial_t* const* partials, int n_shards, int64_t T,
                            const uint8_t* active_mask, float* out_logprob, float* out_lse,

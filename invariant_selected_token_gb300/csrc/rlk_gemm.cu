@@ -321,8 +321,6 @@ __global__ void k_sum_splits(const float* parts, int64_t split_stride, int split
 
 }  // namespace
 
-int gemm_smem_bytes() { return kSmemBytes; }
-
 cudaError_t prepare_gemm_kernels() {
     cudaError_t e;
     if ((e = cudaFuncSetAttribute(k_gemm_f32<false, true>,

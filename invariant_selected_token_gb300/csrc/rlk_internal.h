@@ -45,7 +45,6 @@ enum TileEpilogue { kEpiPartials = 0, kEpiDebugLogits = 1, kEpiGrad = 2 };
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
                                  const TilePartialsArgs& a, int epilogue, int num_sms,
                                  cudaStream_t stream);
-int tile_partials_smem_bytes();
 cudaError_t prepare_tile_partials_kernels();
 
 struct TileTreeArgs {

@@ -64,11 +64,9 @@ constexpr int smem_bytes_of() {
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;
 __host__ __device__ constexpr int ring_stages(int a_rows, bool grad) {
-    return (kSmemLimit - 1024 - 256 - (grad ? static_cast<int>(kGradStageBytes) : 0)) /
-                       (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB)) > kMaxStages
-               ? kMaxStages
-               : (kSmemLimit - 1024 - 256 - (grad ? static_cast<int>(kGradStageBytes) : 0)) /
-                     (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB));
+    const int budget = kSmemLimit - 1024 - 256 - (grad ? static_cast<int>(kGradStageBytes) : 0);
+    const int n = budget / (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB));
+    return n > kMaxStages ? kMaxStages : n;
 }
 template <int kEpi>
 constexpr int ring_smem_bytes(int a_rows) {
@@ -466,8 +464,6 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
 }
 
 }  // namespace
-
-int tile_partials_smem_bytes() { return kSmemBytes; }
 
 cudaError_t prepare_tile_partials_kernels() {
     cudaError_t e;
