@@ -87,7 +87,7 @@ def test_vocab_ranks_match_the_unsharded_call(rlk, cuda_device, case, world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, case, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, case, q), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted((q.get(timeout=600) for _ in range(world)), key=lambda x: x[0])

@@ -104,7 +104,7 @@ def test_vocab_parallel_exchange_on_gloo_ranks(world):
     port = _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted((q.get(timeout=120) for _ in range(world)), key=lambda x: x[0])
@@ -137,7 +137,7 @@ def test_gather_records_rank_order():
     world, port = 4, _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_gather_main, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_gather_main, args=(r, world, port, q), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = [q.get(timeout=120) for _ in range(world)]
@@ -170,7 +170,7 @@ def test_rank_leaving_before_exchange_fails_the_peer_not_hangs():
     world, port = 2, _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_failing_main, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_failing_main, args=(r, world, port, q), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=120) for _ in range(world))
@@ -198,7 +198,7 @@ def test_group_of_three_ranks_is_refused():
     world, port = 3, _free_port()
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    procs = [ctx.Process(target=_three_main, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_three_main, args=(r, world, port, q), daemon=True) for r in range(world)]
     for p in procs:
         p.start()
     res = dict(q.get(timeout=120) for _ in range(world))
