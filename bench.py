@@ -47,7 +47,7 @@ def parse():
                    choices=["packed", "decode1", "decode8", "decode64", "decode128", "decode256",
                             "decode512",
                             "logits_fp32", "logits_bf16", "log_softmax_fp32", "backward", "grpo",
-                            "rmsnorm", "sweep"],
+                            "rmsnorm", "rmsnorm16k", "sweep"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path; "
@@ -55,7 +55,8 @@ def parse():
                         "backward: the deterministic backward of the packed batch; grpo: the "
                         "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls); "
                         "rmsnorm: the strict RMSNorm (residual in and out) that produces the "
-                        "packed batch's hidden states; sweep: tokens/s against batch size on the "
+                        "packed batch's hidden states (L2 flushed between calls); rmsnorm16k: the "
+                        "same on 16384 rows, inputs larger than L2 and no flush; sweep: tokens/s against batch size on the "
                         "8192-token sweep set")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -679,9 +680,12 @@ def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
     """The strict RMSNorm producing the head's hidden states for the packed batch: residual
     add (bf16 residual stream out) and normalisation, T = 4096, H = 4096.  Its four
     [T, H] bf16 tensors (134 MB) are about L2's size, so L2 is flushed (a 512 MB write)
-    between timed calls, outside the timed interval."""
+    between timed calls, outside the timed interval.  The write leaves L2 full of dirty
+    lines that the call's reads must first write back.  rmsnorm16k: T = 16384 rows, whose
+    tensors (537 MB) are larger than L2, with no flush."""
     import torch
-    T = T_PACKED
+    big = args.workload == "rmsnorm16k"
+    T = 4 * T_PACKED if big else T_PACKED
     g = torch.Generator(device=dev)
     g.manual_seed(4242 + 1000 * rank)
     x = (torch.randn((T, H), generator=g, device=dev) * 2.0).to(torch.bfloat16)
@@ -689,7 +693,7 @@ def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
     gamma = (1.0 + 0.1 * torch.randn((H,), generator=g, device=dev)).to(torch.bfloat16)
     out = torch.empty_like(x)
     res_out = torch.empty_like(x)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = None if big else torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def call():
@@ -709,7 +713,8 @@ def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
     time.sleep(0.3)
     t0 = time.time()
     for a, b in ev:
-        flush.fill_(1)
+        if flush is not None:
+            flush.fill_(1)
         a.record(stream)
         call()
         b.record(stream)
@@ -726,10 +731,15 @@ def rmsnorm_arm(args, rank, world, dev, dist, binding, WL):
                     "warmup": max(3, args.warmup), "ms_per_step": call_ms,
                     "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                     "dtype": "bf16", "data": "synthetic",
-                    "config": {"workload": "strict RMSNorm with residual add of the packed batch "
-                                           "(T=4096, H=4096, bf16 in/out, eps 1e-6)",
+                    "config": {"workload": ("strict RMSNorm with residual add, T=16384 rows "
+                                            "(4 packed batches), H=4096, bf16 in/out, eps 1e-6")
+                                           if big else
+                                           ("strict RMSNorm with residual add of the packed batch "
+                                            "(T=4096, H=4096, bf16 in/out, eps 1e-6)"),
                                "T": T, "H": H,
-                               "l2": "flushed between calls (512 MB write outside the timed "
+                               "l2": ("inputs larger than L2 (4 x %.0f MB), no flush"
+                                      % (T * H * 2 / 1e6)) if big else
+                                     "flushed between calls (512 MB write outside the timed "
                                      "interval)"},
                     "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -831,7 +841,7 @@ def main():
         dist.barrier()
     binding.lib()
 
-    if args.workload == "rmsnorm":
+    if args.workload in ("rmsnorm", "rmsnorm16k"):
         return rmsnorm_arm(args, rank, world, dev, dist, binding, WL)
     W = WL.head_weights(dev)                       # same weights on every rank
     if args.workload == "grpo":
