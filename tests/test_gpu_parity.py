@@ -94,11 +94,12 @@ def test_qwen_packed_sampled_rows(rlk, qwen):
     assert 10.0 < np.median(ref_lse) < 16.0
 
 
-@pytest.mark.parametrize("n", [1, 64])
+@pytest.mark.parametrize("n", [1, 64, 256])
 def test_qwen_decode_rows_against_oracle(rlk, qwen, n):
     """Decode batches as the rollout side issues them (T = 1 and T = 64 rows of the packed
-    batch, the single-token-tile schedule with a shrunk hidden box), every row against the
-    oracle directly -- not only through their bitwise equality with the packed rows."""
+    batch: one token tile with a shrunk hidden box and a deeper ring; T = 256: two token
+    tiles sharing each W tile), every row against the oracle directly -- not only through
+    their bitwise equality with the packed rows."""
     pk = qwen.packed
     rows = WL.decode_rows(n)
     idx = torch.from_numpy(rows).to(qwen.device)
