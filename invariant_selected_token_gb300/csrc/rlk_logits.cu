@@ -194,32 +194,54 @@ __device__ __forceinline__ UnitCoords unit_coords(int unit, int num_n, int num_m
     return c;
 }
 
-// kFullBox: the hidden box is a full 128-row token tile (batches of more than
-// 128 tokens): the ring is the fixed 4 x 48 KB one.  Otherwise the box holds
-// roundup(T, 8) rows and the ring is sized by ring_stages.
-template <int kEpi, bool kFullBox>
+// Shared-memory rings of the logits kernel:
+//   kRingFull   full 128-row hidden boxes, one ring of 4 (hidden, W) stages;
+//   kRingSmall  hidden boxes of roundup(T, 8) < 128 rows (decode batches), one
+//               ring of ring_stages() stages;
+//   kRingSplit  full hidden boxes in a ring of 4 and W boxes in a ring of 5,
+//               filled independently as their slots free up (W first), for
+//               batches of two token tiles (128 < T <= 256): each W tile is then
+//               shared by two CTAs and streamed from HBM while their MMAs run at
+//               the same pace, and the extra W stage of lookahead pays
+//               (232 -> 224 us at T = 256); at the tensor-bound sizes it cost
+//               8 %, so no other size uses it.  Not with the backward's G
+//               staging rows, which leave no room for the fifth W stage.
+enum RingKind { kRingFull = 0, kRingSmall = 1, kRingSplit = 2 };
+constexpr int kSplitStagesB = kStages + 1;
+constexpr int kSplitSmemBytes = kStages * static_cast<int>(kStageBytesA) +
+                                kSplitStagesB * static_cast<int>(kStageBytesB) + 1024 + 256;
+static_assert(kSplitSmemBytes <= kSmemLimit, "split rings exceed shared memory");
+
+template <int kEpi, int kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     k_tile_partials(const __grid_constant__ CUtensorMap map_hidden,
                     const __grid_constant__ CUtensorMap map_w, const TilePartialsArgs a) {
+    constexpr bool kSplit = kRing == kRingSplit;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     // hidden slots are a_box_rows rows each; the MMA still reads 128 rows from a
     // slot, and the rows past the box (the next slots' or the W boxes' bytes,
     // inside this allocation) only feed accumulator rows that are never read
-    const int S = kFullBox ? kStages : ring_stages(a.a_box_rows, kEpi == kEpiGrad);
-    const uint32_t a_stage =
-        kFullBox ? kStageBytesA : static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2;
+    const int S = kRing == kRingSmall ? ring_stages(a.a_box_rows, kEpi == kEpiGrad) : kStages;
+    const int SB = kSplit ? kSplitStagesB : S;  // W slots
+    const uint32_t a_stage = kRing == kRingSmall
+                                 ? static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2
+                                 : kStageBytesA;
     uint8_t* sA = smem;
     uint8_t* sB = smem + S * a_stage;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * kStageBytesB);
+    // full/empty: the (hidden, W) stages, or the hidden ring alone when split;
+    // fullB/emptyB: the W ring when split
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + SB * kStageBytesB);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* acc_full = empty + kMaxStages;
+    uint64_t* fullB = empty + kMaxStages;
+    uint64_t* emptyB = fullB + kMaxStages;
+    uint64_t* acc_full = emptyB + kMaxStages;
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // backward only: per-epilogue-warp staging rows for the G stores
-    uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + S * kStageBytesB + 256);
+    uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + SB * kStageBytesB + 256);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -235,6 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
+        if (kSplit)
+            for (int s = 0; s < SB; ++s) {
+                ptx::mbar_init(&fullB[s], 1);
+                ptx::mbar_init(&emptyB[s], 1);
+            }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
             ptx::mbar_init(&acc_empty[b], 4 * 32);
@@ -257,7 +284,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dependency_wait();
 
     if (warp == 0) {
-        if (lane == 0) {
+        if (lane == 0 && kSplit) {
+            // ---------------- TMA producer, split rings: each ring is refilled as
+            // soon as one of its slots is free (W first), so the W stream runs up
+            // to five stages ahead of the MMAs and the hidden rows up to four.
+            uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
+            if (a.test_drop_stage && blockIdx.x == 0) {
+                // test only: leave hidden slot 0 unfilled; the MMA's bounded wait gives up
+                sa = 1;
+            }
+            int ua = unit0, ka = 0, ub = unit0, kbb = 0;  // next k-block of each ring
+            UnitCoords ca = unit_coords(ua, num_n, num_m, kBandTokenTiles);
+            UnitCoords cb = ca;
+            bool idle = false;
+            uint64_t t_idle = 0;
+            while ((ua < total || ub < total) && !*abort_flag) {
+                bool did = false;
+                if (ub < total && ptx::mbar_try_wait(ptx::smem_addr(&emptyB[sb]), pb ^ 1u)) {
+                    ptx::mbar_arrive_expect_tx(&fullB[sb], kStageBytesB);
+                    ptx::tma_load_2d(sB + sb * kStageBytesB, &map_w, &fullB[sb], kbb * kBlockK,
+                                     cb.n_blk * kTileN);
+                    if (++sb == static_cast<uint32_t>(SB)) {
+                        sb = 0;
+                        pb ^= 1u;
+                    }
+                    if (++kbb == a.k_blocks) {
+                        kbb = 0;
+                        ub += ustride;
+                        if (ub < total) cb = unit_coords(ub, num_n, num_m, kBandTokenTiles);
+                    }
+                    did = true;
+                }
+                if (ua < total && ptx::mbar_try_wait(ptx::smem_addr(&empty[sa]), pa ^ 1u)) {
+                    ptx::mbar_arrive_expect_tx(&full[sa], kStageBytesA);
+                    ptx::tma_load_2d(sA + sa * kStageBytesA, &map_hidden, &full[sa], ka * kBlockK,
+                                     ca.mu * kTileM);
+                    if (++sa == static_cast<uint32_t>(S)) {
+                        sa = 0;
+                        pa ^= 1u;
+                    }
+                    if (++ka == a.k_blocks) {
+                        ka = 0;
+                        ua += ustride;
+                        if (ua < total) ca = unit_coords(ua, num_n, num_m, kBandTokenTiles);
+                    }
+                    did = true;
+                }
+                if (did) {
+                    idle = false;
+                } else if (!idle) {
+                    idle = true;
+                    t_idle = ptx::globaltimer();
+                } else if (ptx::globaltimer() - t_idle > ptx::kWaitLimitNs) {
+                    *abort_flag = 1;
+                    report(a.status, RLK_ERR_TIMEOUT);
+                    break;
+                }
+            }
+        } else if (lane == 0) {
             // ---------------- TMA producer
             // A batch of at most 128 tokens loads only its first roundup(T, 8)
             // hidden rows; the accumulator rows beyond them are never read.
@@ -291,8 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // ---------------- MMA issuer
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            // ---------------- MMA issuer (split rings: stage/phase track the hidden
+            // ring, sb/pb the W ring)
+            uint32_t stage = 0, phase = 0, sb = 0, pb = 0, acc = 0, acc_phase = 0;
             for (int unit = unit0; unit < total && !*abort_flag; unit += ustride) {
                 if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag)) {
                     *abort_flag = 1;
@@ -303,13 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + acc * kTileN;
                 bool ok = true;
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) {
+                    if ((kSplit && !ptx::mbar_wait(&fullB[sb], pb, abort_flag)) ||
+                        !ptx::mbar_wait(&full[stage], phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
                     const uint32_t a0 = ptx::smem_addr(sA + stage * a_stage);
-                    const uint32_t b0 = ptx::smem_addr(sB + stage * kStageBytesB);
+                    const uint32_t b0 = ptx::smem_addr(sB + (kSplit ? sb : stage) * kStageBytesB);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzle row
@@ -321,6 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++stage == static_cast<uint32_t>(S)) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    if (kSplit) {
+                        ptx::mma_commit(&emptyB[sb]);
+                        if (++sb == static_cast<uint32_t>(SB)) {
+                            sb = 0;
+                            pb ^= 1u;
+                        }
                     }
                 }
                 if (!ok) {
@@ -434,11 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int kEpi>
 cudaError_t set_smem_attr() {
-    const cudaError_t e = cudaFuncSetAttribute(
-        k_tile_partials<kEpi, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_of<kEpi>());
+    cudaError_t e = cudaFuncSetAttribute(k_tile_partials<kEpi, kRingFull>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes_of<kEpi>());
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_tile_partials<kEpi, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    e = cudaFuncSetAttribute(k_tile_partials<kEpi, kRingSmall>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if constexpr (kEpi != kEpiGrad) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_tile_partials<kEpi, kRingSplit>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmemBytes);
+    }
+    return e;
 }
 
 template <int kEpi>
@@ -451,16 +551,25 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    const bool full_box = a.a_box_rows == kTileM;
-    cfg.dynamicSmemBytes = full_box ? smem_bytes_of<kEpi>() : ring_smem_bytes<kEpi>(a.a_box_rows);
+    const int ring = a.a_box_rows < kTileM ? kRingSmall
+                     : (num_m == 2 && kEpi != kEpiGrad) ? kRingSplit
+                                                         : kRingFull;
+    cfg.dynamicSmemBytes = ring == kRingSmall ? ring_smem_bytes<kEpi>(a.a_box_rows)
+                           : ring == kRingSplit ? kSplitSmemBytes
+                                                : smem_bytes_of<kEpi>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return full_box ? cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, true>, map_hidden, map_w, a)
-                    : cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, false>, map_hidden, map_w, a);
+    if (ring == kRingSmall)
+        return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, kRingSmall>, map_hidden, map_w, a);
+    if constexpr (kEpi != kEpiGrad) {
+        if (ring == kRingSplit)
+            return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, kRingSplit>, map_hidden, map_w, a);
+    }
+    return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, kRingFull>, map_hidden, map_w, a);
 }
 
 }  // namespace
