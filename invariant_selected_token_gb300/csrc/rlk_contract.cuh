@@ -110,6 +110,12 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 // low bits of t directly: with t = 1.5 * 2^23 + n exactly, the scalar's
 // (bits(t) - bits(1.5 * 2^23) + 127) << 23 equals bits(t) * 2^23 + bits(1.0f)
 // modulo 2^32, because bits(1.5 * 2^23) * 2^23 vanishes modulo 2^32.
+// kUnderflow = false is for arguments known to lie in [-86, 0] (numbers, not
+// NaN): no select is needed, and since p is a normal number in [0.7, 1.5]
+// and n >= -124, p * 2^n is normal and exact, i.e. n added to p's exponent
+// field -- bits(p) + bits(t) * 2^23 modulo 2^32 (same reasoning as for the
+// scale) -- one integer multiply-add instead of forming 2^n and multiplying.
+template <bool kUnderflow = true>
 __device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
     const uint64_t t = f2_fma(x, f2_splat(0x1.715476p+0f), f2_splat(0x1.8p+23f));
     const uint64_t n = f2_add(t, f2_splat(-0x1.8p+23f));
@@ -124,6 +130,12 @@ __device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
     p = f2_fma(p, r, f2_splat(1.0f));
     float tl, th;
     f2_unpack(t, tl, th);
+    if (!kUnderflow) {
+        float pl, ph;
+        f2_unpack(p, pl, ph);
+        return f2_pack(__uint_as_float(__float_as_uint(pl) + __float_as_uint(tl) * 8388608u),
+                       __uint_as_float(__float_as_uint(ph) + __float_as_uint(th) * 8388608u));
+    }
     const uint64_t scale = f2_pack(__uint_as_float(__float_as_uint(tl) * 8388608u + 0x3F800000u),
                                    __uint_as_float(__float_as_uint(th) * 8388608u + 0x3F800000u));
     float yl, yh, xl, xh;
@@ -183,6 +195,31 @@ __device__ __forceinline__ MaxSum contract_merge(MaxSum left, MaxSum right) {
 // levels 2-6 run this way and level 7 adds the two halves.  The packed
 // levels are evaluated as a binary counter over j (a node is formed as soon
 // as both children exist), which keeps few partial sums live.
+struct TreeX2 {
+    uint64_t pending[5];  // pending[L]: a finished left node of packed level L + 2
+    uint64_t x = 0;
+    // the exps of pairs j and j + 32 (columns 2j, 2j+1 and 64+2j, 64+2j+1), in
+    // order j = 0..31; j must be a compile-time constant after unrolling
+    __device__ __forceinline__ void push(int j, uint64_t e_lo, uint64_t e_hi) {
+        float a, b, c, d;
+        f2_unpack(e_lo, a, b);
+        f2_unpack(e_hi, c, d);
+        x = f2_pack(__fadd_rn(a, b), __fadd_rn(c, d));  // X_j
+        int level = 0;
+#pragma unroll
+        for (; level < 5; ++level) {
+            if (!(j & (1 << level))) break;
+            x = f2_add(pending[level], x);  // left sibling + this node
+        }
+        if (level < 5) pending[level] = x;
+    }
+    __device__ __forceinline__ float total() const {
+        float z0, z1;
+        f2_unpack(x, z0, z1);  // the two 64-column halves
+        return __fadd_rn(z0, z1);
+    }
+};
+
 __device__ __forceinline__ MaxSum tile_reduce_x2(uint64_t (&P)[64]) {
     float m0, m1, m2, m3;
     f2_unpack(P[0], m0, m1);
@@ -199,27 +236,13 @@ __device__ __forceinline__ MaxSum tile_reduce_x2(uint64_t (&P)[64]) {
     }
     const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
     const uint64_t neg_m = f2_splat(-m);
-    uint64_t pending[5];  // pending[L]: a finished left node of packed level L + 2
-    uint64_t x = 0;
+    TreeX2 tree;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        float a, b, c, d;
-        f2_unpack(contract_exp_x2(f2_add(P[j], neg_m)), a, b);
-        f2_unpack(contract_exp_x2(f2_add(P[j + 32], neg_m)), c, d);
-        x = f2_pack(__fadd_rn(a, b), __fadd_rn(c, d));  // X_j
-        int level = 0;
-#pragma unroll
-        for (; level < 5; ++level) {
-            if (!(j & (1 << level))) break;
-            x = f2_add(pending[level], x);  // left sibling + this node
-        }
-        if (level < 5) pending[level] = x;
-    }
-    float z0, z1;
-    f2_unpack(x, z0, z1);  // the two 64-column halves
+    for (int j = 0; j < 32; ++j)
+        tree.push(j, contract_exp_x2(f2_add(P[j], neg_m)), contract_exp_x2(f2_add(P[j + 32], neg_m)));
     MaxSum out;
     out.m = m;
-    out.s = __fadd_rn(z0, z1);
+    out.s = tree.total();
     return out;
 }
 

@@ -126,30 +126,101 @@ __device__ __forceinline__ void stage_wait() {
     __syncwarp();
 }
 
-// A staged tile as 64 fp32 pairs (columns 2k, 2k+1; bf16 widens exactly).
-template <int kDtype>
-__device__ __forceinline__ void read_tile_pairs(const void* sm_raw, int tile, uint64_t (&P)[64]) {
-    constexpr int kPitch = Pitch<kDtype>::value;
-    if (kDtype == RLK_DTYPE_F32) {
-        const float* p = static_cast<const float*>(sm_raw) + tile * kPitch;
+// A staged fp32 tile as 64 pairs (columns 2k, 2k+1).
+__device__ __forceinline__ void read_tile_pairs_f32(const void* sm_raw, int tile, uint64_t (&P)[64]) {
+    const float* p = static_cast<const float*>(sm_raw) + tile * Pitch<RLK_DTYPE_F32>::value;
 #pragma unroll
-        for (int c = 0; c < kVocabTile; c += 4) {
-            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(p + c);
-            P[c / 2] = q.x;
-            P[c / 2 + 1] = q.y;
-        }
-    } else {
-        const uint16_t* p = static_cast<const uint16_t*>(sm_raw) + tile * kPitch;
+    for (int c = 0; c < kVocabTile; c += 4) {
+        const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(p + c);
+        P[c / 2] = q.x;
+        P[c / 2 + 1] = q.y;
+    }
+}
+
+// Eight staged bf16 values (16 bytes) as four words; the asm keeps each read
+// where it stands, so no tile is held in registers between the two passes.
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 q;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(q.x), "=r"(q.y), "=r"(q.z), "=r"(q.w)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))));
+    return q;
+}
+
+// A bf16 word (two columns) widened exactly to an fp32 pair.
+__device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w) {
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) {
+    __nv_bfloat162 b;
+    memcpy(&b, &w, 4);
+    return b;
+}
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 b) {
+    uint32_t w;
+    memcpy(&w, &b, 4);
+    return w;
+}
+
+// Second pass over a staged bf16 tile: the packed tree of the exps, reading
+// pairs j..j+3 and j+32..j+35 as they are needed.
+template <bool kUnderflow>
+__device__ __forceinline__ float bf16_tile_sum(const uint16_t* tile, uint64_t neg_m) {
+    TreeX2 tree;
 #pragma unroll
-        for (int c = 0; c < kVocabTile; c += 8) {
-            const uint4 q = *reinterpret_cast<const uint4*>(p + c);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int j0 = 0; j0 < 32; j0 += 4) {
+        const uint4 lo = lds128(tile + 2 * j0);
+        const uint4 hi = lds128(tile + 64 + 2 * j0);
+        const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
+        const uint32_t H[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                P[c / 2 + i] = f2_pack(__uint_as_float(w[i] << 16),
-                                       __uint_as_float(w[i] & 0xFFFF0000u));
+        for (int i = 0; i < 4; ++i)
+            tree.push(j0 + i, contract_exp_x2<kUnderflow>(f2_add(widen_bf16x2(L[i]), neg_m)),
+                      contract_exp_x2<kUnderflow>(f2_add(widen_bf16x2(H[i]), neg_m)));
+    }
+    return tree.total();
+}
+
+// A staged bf16 tile reduced straight from shared memory in two passes: max
+// and min two columns per instruction on the bf16 pairs (bf16 widens
+// exactly and monotonically, so the widened max is the fp32 max of the
+// widened values; the min propagates NaN), then the exps and the tree.
+// When the tile holds no NaN and its smallest value is within 86 of its max,
+// every exp argument lies in [-86, 0] and the exps take their shorter form
+// (no underflow select, the scaling by 2^n an exponent add); the bits are
+// the same either way.
+__device__ __forceinline__ MaxSum bf16_tile_reduce(const uint16_t* tile) {
+    __nv_bfloat162 mx[2], mn[2];
+#pragma unroll
+    for (int c = 0; c < kVocabTile; c += 8) {
+        const uint4 q = lds128(tile + c);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 b = as_bf162(w[i]);
+            if (c == 0 && i < 2) {
+                mx[i] = b;
+                mn[i] = b;
+            } else {
+                mx[i & 1] = __hmax2(mx[i & 1], b);
+                mn[i & 1] = __hmin2_nan(mn[i & 1], b);
+            }
         }
     }
+    const uint64_t mx2 = widen_bf16x2(as_u32(__hmax2(mx[0], mx[1])));
+    const uint64_t mn2 = widen_bf16x2(as_u32(__hmin2_nan(mn[0], mn[1])));
+    float a, b, c, d;
+    f2_unpack(mx2, a, b);
+    f2_unpack(mn2, c, d);
+    MaxSum out;
+    out.m = fmaxf(a, b);
+    const uint64_t neg_m = f2_splat(-out.m);
+    // NaN in c or d (or a NaN difference) fails the comparison
+    if (__fsub_rn(c, out.m) >= -86.0f && __fsub_rn(d, out.m) >= -86.0f)
+        out.s = bf16_tile_sum<false>(tile, neg_m);
+    else
+        out.s = bf16_tile_sum<true>(tile, neg_m);
+    return out;
 }
 
 // Staged element c of a tile as fp32.
@@ -160,10 +231,15 @@ __device__ __forceinline__ float staged_value(const void* sm_raw, int tile, int 
     return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(sm_raw)[tile * kPitch + c]) << 16);
 }
 
-// Three CTAs per SM: the fp32 slices fill shared memory at three, and the
-// register cap (168) that three imply costs no spills.
+// fp32: three CTAs per SM -- the slices fill shared memory at three, and the
+// register cap (168) that three imply costs no spills.  bf16: six CTAs per
+// SM -- the tile is reduced from shared memory, not held in registers, and
+// the other warps cover a warp's staging.
 template <int kDtype>
-__global__ void __launch_bounds__(kMatWarps * 32, 3)
+constexpr int mat_ctas_per_sm() { return kDtype == RLK_DTYPE_F32 ? 3 : 6; }
+
+template <int kDtype>
+__global__ void __launch_bounds__(kMatWarps * 32, mat_ctas_per_sm<kDtype>())
     k_mat_tile_partials(const void* logits, int64_t ld, bool vec, const int32_t* targets,
                         const uint8_t* active, int T, int V, int n_tiles, float2* partials,
                         float* tgt_logit) {
@@ -209,18 +285,31 @@ __global__ void __launch_bounds__(kMatWarps * 32, 3)
         const int j = s * kSliceTiles + lane;
         const bool own = j < n_tiles;
         const int ncols = own ? min(kVocabTile, V - j * kVocabTile) : 0;
-        uint64_t P[64];
-        if (own) {
-            if (targets) {
-                const int64_t tl = static_cast<int64_t>(targets[t]) - static_cast<int64_t>(j) * kVocabTile;
-                if (tl >= 0 && tl < ncols) tgt_logit[t] = staged_value<kDtype>(sm, lane, static_cast<int>(tl));
-            }
-            read_tile_pairs<kDtype>(sm, lane, P);
+        if (own && targets) {
+            const int64_t tl = static_cast<int64_t>(targets[t]) - static_cast<int64_t>(j) * kVocabTile;
+            if (tl >= 0 && tl < ncols) tgt_logit[t] = staged_value<kDtype>(sm, lane, static_cast<int>(tl));
         }
-        __syncwarp();  // every lane has its tile: the buffer is free
         int nt = t, ns = s;
         advance(nt, ns);
         skip_inactive(nt, ns);
+        if constexpr (kDtype == RLK_DTYPE_BF16) {
+            if (own) {
+                // columns past the vocabulary are not part of the tile: -inf
+                // (bf16 0xFF80) in the lane's own staged tile
+                uint16_t* tile = static_cast<uint16_t*>(sm) + lane * Pitch<kDtype>::value;
+                for (int c = ncols; c < kVocabTile; ++c) tile[c] = 0xFF80u;
+                const MaxSum r = bf16_tile_reduce(tile);
+                partials[static_cast<int64_t>(t) * n_tiles + j] = make_float2(r.m, r.s);
+            }
+            __syncwarp();  // every lane is done with its tile: the buffer is free
+            if (nt < T) issue(nt, ns);
+            t = nt;
+            s = ns;
+            continue;
+        }
+        uint64_t P[64];
+        if (own) read_tile_pairs_f32(sm, lane, P);
+        __syncwarp();  // every lane has its tile: the buffer is free
         if (nt < T) issue(nt, ns);
         if (own) {
             // columns past the vocabulary are not part of the tile: -inf, whose
@@ -266,8 +355,12 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// fp32 slices are the larger: 4 warps x 32 tiles x 132 x 4 B = 66 KB, 3 CTAs per SM
-constexpr int kMatSmem = kMatWarps * kSliceTiles * Pitch<RLK_DTYPE_F32>::value * 4;
+// one slice per warp: fp32 4 warps x 32 tiles x 132 x 4 B = 66 KB (3 CTAs per
+// SM), bf16 4 x 32 x 136 x 2 B = 34 KB (6 CTAs per SM)
+template <int kDtype>
+constexpr int mat_smem_bytes() {
+    return kMatWarps * kSliceTiles * Pitch<kDtype>::value * (kDtype == RLK_DTYPE_F32 ? 4 : 2);
+}
 
 // Every row starts on a 16-byte boundary (16-byte copies of whole chunks).
 bool rows_vector_aligned(const void* logits, int dtype, int64_t ld) {
@@ -279,16 +372,20 @@ bool rows_vector_aligned(const void* logits, int dtype, int64_t ld) {
 
 cudaError_t prepare_mat_kernels(int* ctas_per_sm) {
     cudaError_t e = cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_F32>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         mat_smem_bytes<RLK_DTYPE_F32>());
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_mat_tile_partials<RLK_DTYPE_BF16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMatSmem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mat_smem_bytes<RLK_DTYPE_BF16>());
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &ctas_per_sm[0], k_mat_tile_partials<RLK_DTYPE_F32>, kMatWarps * 32, kMatSmem);
+            &ctas_per_sm[0], k_mat_tile_partials<RLK_DTYPE_F32>, kMatWarps * 32,
+            mat_smem_bytes<RLK_DTYPE_F32>());
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &ctas_per_sm[1], k_mat_tile_partials<RLK_DTYPE_BF16>, kMatWarps * 32, kMatSmem);
+            &ctas_per_sm[1], k_mat_tile_partials<RLK_DTYPE_BF16>, kMatWarps * 32,
+            mat_smem_bytes<RLK_DTYPE_BF16>());
     if (e == cudaSuccess && (ctas_per_sm[0] < 1 || ctas_per_sm[1] < 1)) e = cudaErrorInvalidConfiguration;
     return e;
 }
@@ -303,12 +400,12 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
     int64_t blocks = (tasks + kMatWarps - 1) / kMatWarps;
     if (blocks > resident_ctas) blocks = resident_ctas;
     if (dtype == RLK_DTYPE_F32)
-        k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32, kMatSmem,
-                                             stream>>>(logits, ld, vec, targets, active, T, V,
+        k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32,
+                                             mat_smem_bytes<RLK_DTYPE_F32>(), stream>>>(logits, ld, vec, targets, active, T, V,
                                                        n_tiles, partials, tgt_logit);
     else
-        k_mat_tile_partials<RLK_DTYPE_BF16><<<static_cast<int>(blocks), kMatWarps * 32, kMatSmem,
-                                              stream>>>(logits, ld, vec, targets, active, T, V,
+        k_mat_tile_partials<RLK_DTYPE_BF16><<<static_cast<int>(blocks), kMatWarps * 32,
+                                              mat_smem_bytes<RLK_DTYPE_BF16>(), stream>>>(logits, ld, vec, targets, active, T, V,
                                                         n_tiles, partials, tgt_logit);
     return cudaGetLastError();
 }

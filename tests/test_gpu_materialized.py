@@ -83,6 +83,46 @@ def test_bf16_logits_and_log_softmax(rlk, cuda_device, T, V, seed):
     assert np.abs(out.cpu().numpy() - ref).max() <= 1e-4 * (1 + np.abs(ref).max() / 100)
 
 
+def test_bf16_logits_wide_range_underflow(rlk, cuda_device):
+    """bf16 tiles whose values reach below max - 86, where the contract's exp gives +0:
+    such tiles take the exps with the underflow select, tiles within 86 of their max
+    take them without it, and the bits must not depend on which.  Planted rows put a
+    tile's smallest value at exactly max - 86 (no select needed), one bf16 step below
+    it (select needed), at -inf, and at both signs of zero."""
+    T, V = 40, 3000
+    L, tg = cpu_logits(T, V, 31, scale=40.0)
+    L[T // 2:] *= np.float32(0.075)  # the second half's tiles stay within 86 of their max
+    L[0, :128] = 0.0
+    L[0, 5] = -86.0
+    L[1, :128] = 1.0
+    L[1, 7] = -85.5            # RN(-85.5 - 1) = -86.5: below -86 by one bf16 step of 86
+    L[2, 128:256] = -3.0
+    L[2, 200] = -np.inf
+    L[3, :128] = np.where(np.arange(128) % 2 == 0, 0.0, -0.0)
+    L[4, 256:384] = 2.0
+    L[4, 300] = -84.0          # RN(-84 - 2) = -86 exactly
+    Lb = WL.f32_to_bf16_bits(L)
+    Lw = WL.bf16_bits_to_f32(Lb)
+    assert Lw[1, 7] == np.float32(-85.5) and Lw[0, 5] == np.float32(-86.0)
+    dLb = torch.from_numpy(Lb.view(np.int16)).view(torch.bfloat16).to(cuda_device)
+    dtg = torch.from_numpy(tg).to(cuda_device)
+    for n in (1, 4):
+        emu = E.linear_logprob(Lw, tg, None, n_shards=n)
+        ws = rlk.new_workspace(T, V, n, cuda_device)
+        lp, lse = rlk.logits_logprob(dLb, dtg, None, n, workspace=ws)
+        same_bits(lp.cpu().numpy(), emu["logprob"], "wide bf16 logprob n=%d" % n)
+        same_bits(lse.cpu().numpy(), emu["lse"], "wide bf16 lse n=%d" % n)
+        rec = rlk.workspace_records(ws, T, V, n).cpu().numpy()
+        same_bits(rec[..., 0].view(np.float32), emu["rec_m"], "wide record m")
+        same_bits(rec[..., 1].view(np.float32), emu["rec_s"], "wide record s")
+    out, lse2 = rlk.log_softmax(dLb)
+    e_out, e_lse = E.log_softmax(Lw)
+    same_bits(lse2.cpu().numpy(), e_lse, "wide log_softmax lse")
+    same_bits(out.cpu().numpy(), e_out, "wide log_softmax values")
+    ref_lp, ref_lse = O.lse_and_logprob_from_logits(Lw.astype(np.float64), tg, None)
+    assert np.abs(lp.cpu().numpy() - ref_lp).max() <= 1e-4 * (1 + np.abs(ref_lp).max() / 100)
+
+
 def test_fp32_log_softmax_masked_and_strided(rlk, cuda_device):
     T, V = 50, 1000
     L, _ = cpu_logits(T, V, 21)
