@@ -39,6 +39,26 @@ def test_exp_exhaustive_accuracy():
     assert max_ulp < 1.0, (max_ulp, worst)
 
 
+def test_exp_scaling_by_exponent_add():
+    """The exp's shorter form for arguments known to lie in [-86, 0]: there n, the nearest
+    integer to x·log2(e), is in [-124, 0] and p = e^r (|r| <= ln2/2, so p in [0.707, 1.415]
+    after rounding) is normal, hence p·2^n is normal and exact, and its bits are
+    bits(p) + n·2^23.  Checked for every fp32 p in [0.7, 1.42] and every such n."""
+    from fractions import Fraction
+    log2e = Fraction(float.fromhex("0x1.715476p+0"))  # the exp's log2(e), an fp32 value
+    for x, n_expected in ((-86, -124), (0, 0)):
+        assert round(Fraction(x) * log2e) == n_expected
+    assert abs(Fraction(-86) * log2e - (-124)) < Fraction(1, 2) - Fraction(1, 100)
+    lo = np.float32(0.7).view(np.uint32)
+    hi = np.float32(1.42).view(np.uint32)
+    p = np.arange(lo, hi + 1, dtype=np.uint32).view(np.float32)
+    pb = p.view(np.uint32)
+    for n in range(-124, 1):
+        prod = (p * np.float32(2.0 ** n)).view(np.uint32)   # one fp32 rounding of p·2^n
+        add = pb + np.uint32((n * (1 << 23)) & 0xFFFFFFFF)  # modulo 2^32
+        assert np.array_equal(prod, add), n
+
+
 def test_log_exhaustive_accuracy():
     """Every fp32 s in [1, 2^21] (the range of a tile-tree sum): within 2 ulp of fp64 log."""
     max_ulp, worst, count = E.log_sweep(1.0, 2.0 ** 21)
