@@ -88,12 +88,13 @@ def test_unaligned_hidden_refused(rlk, cuda_device):
     assert e.value.code == 3
 
 
-@pytest.mark.parametrize("T", [64, 200, 300])
+@pytest.mark.parametrize("T", [64, 120, 200, 300])
 def test_pipeline_wait_gives_up_with_timeout_status(rlk, cuda_device, monkeypatch, T):
     """A pipeline stage that never fills: the bounded wait gives up, the kernel reports
     RLK_ERR_TIMEOUT and returns, and the context stays usable for the next call.  T = 64
-    runs the logits kernel's single ring with a shrunk hidden box, T = 200 its separate
-    hidden and W rings (two token tiles), T = 300 its single ring of full boxes."""
+    and T = 120 run the logits kernel's single ring with a shrunk hidden box (five and four
+    stages), T = 200 its separate hidden and W rings (two token tiles), T = 300 its single
+    ring of full boxes."""
     import time
     w = WL.small_case(T, 256, 1024, seed=12)
     dw = WL.to_device(w, cuda_device)

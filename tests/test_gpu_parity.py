@@ -46,7 +46,7 @@ def test_tiny_all_rows(rlk, cuda_device, n_shards):
 RAGGED = [
     (1, 64, 1, 1), (1, 64, 2, 1), (3, 64, 129, 1), (128, 128, 256, 2), (129, 192, 257, 2),
     (255, 256, 1000, 4), (257, 64, 1024, 8), (300, 128, 5000, 8), (37, 512, 2047, 4),
-    (513, 64, 384, 2), (64, 1024, 12345, 4),
+    (513, 64, 384, 2), (64, 1024, 12345, 4), (112, 256, 3000, 4), (120, 512, 9000, 2),
     # wide hidden sizes: 80, 128 and 1024 K blocks per logit
     (130, 5120, 700, 2), (129, 8192, 1500, 4), (3, 65536, 300, 1),
 ]
