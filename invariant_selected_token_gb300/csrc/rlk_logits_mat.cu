@@ -232,11 +232,12 @@ __device__ __forceinline__ float staged_value(const void* sm_raw, int tile, int 
 }
 
 // fp32: three CTAs per SM -- the slices fill shared memory at three, and the
-// register cap (168) that three imply costs no spills.  bf16: six CTAs per
-// SM -- the tile is reduced from shared memory, not held in registers, and
-// the other warps cover a warp's staging.
+// register cap (168) that three imply costs no spills.  bf16: five CTAs per
+// SM (96 registers) -- the tile is reduced from shared memory,
+// not held in registers, and the other warps cover a warp's staging (four
+// CTAs: 331 us, five: 307 us, six: 308 us at T = 4096).
 template <int kDtype>
-constexpr int mat_ctas_per_sm() { return kDtype == RLK_DTYPE_F32 ? 3 : 6; }
+constexpr int mat_ctas_per_sm() { return kDtype == RLK_DTYPE_F32 ? 3 : 5; }
 
 template <int kDtype>
 __global__ void __launch_bounds__(kMatWarps * 32, mat_ctas_per_sm<kDtype>())
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kMatWarps * 32, mat_ctas_per_sm<kDtype>())
     // (rows, slices) step instead of dividing a task index per task.
     // Inactive rows are skipped.  The row index stays in 32 bits: T is at most
     // RLK_MAX_ROWS = 2^31 - 2^20 and a step passes the last row by less than
-    // one grid stride (far below 2^20 tasks).
+    // one grid stride (at most kMatMaxBlocks * kMatWarps = 2^20 tasks).
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kMatWarps;
     const int step_t = static_cast<int>(stride / slices_per_row);
     const int step_s = static_cast<int>(stride - static_cast<int64_t>(step_t) * slices_per_row);
@@ -362,6 +363,9 @@ constexpr int mat_smem_bytes() {
     return kMatWarps * kSliceTiles * Pitch<kDtype>::value * (kDtype == RLK_DTYPE_F32 ? 4 : 2);
 }
 
+// Largest grid of the materialised-logits kernel (the walk's step bound).
+constexpr int64_t kMatMaxBlocks = int64_t(1) << 18;
+
 // Every row starts on a 16-byte boundary (16-byte copies of whole chunks).
 bool rows_vector_aligned(const void* logits, int dtype, int64_t ld) {
     const int64_t row_bytes = ld * (dtype == RLK_DTYPE_F32 ? 4 : 2);
@@ -398,7 +402,13 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
     const bool vec = rows_vector_aligned(logits, dtype, ld);
     const int64_t tasks = static_cast<int64_t>(T) * ((n_tiles + kSliceTiles - 1) / kSliceTiles);
     int64_t blocks = (tasks + kMatWarps - 1) / kMatWarps;
-    if (blocks > resident_ctas) blocks = resident_ctas;
+    // fp32: one resident wave, each warp overlapping its next slice's copies
+    // with its reduction.  bf16: a warp per task (up to 2^20 tasks per walk
+    // step), so the block scheduler hands out work as warps finish; one
+    // persistent wave with a fixed walk left a quarter of the warp slots
+    // idle on average (348 against 308 us at T = 4096).
+    if (dtype == RLK_DTYPE_F32 && blocks > resident_ctas) blocks = resident_ctas;
+    if (blocks > kMatMaxBlocks) blocks = kMatMaxBlocks;
     if (dtype == RLK_DTYPE_F32)
         k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32,
                                              mat_smem_bytes<RLK_DTYPE_F32>(), stream>>>(logits, ld, vec, targets, active, T, V,
