@@ -407,7 +407,14 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
     // step), so the block scheduler hands out work as warps finish; one
     // persistent wave with a fixed walk left a quarter of the warp slots
     // idle on average (348 against 308 us at T = 4096).
-    if (dtype == RLK_DTYPE_F32 && blocks > resident_ctas) blocks = resident_ctas;
+    if (dtype == RLK_DTYPE_F32 && blocks > resident_ctas) {
+        blocks = resident_ctas;
+        // a walk stride that is a multiple of the slices per row would give
+        // every warp a fixed slice index, and the warps of a row's short last
+        // slice little work (one CTA fewer: 420 -> 417 us at V = 151936)
+        const int64_t slices_per_row = (n_tiles + kSliceTiles - 1) / kSliceTiles;
+        if (blocks > 1 && (blocks * kMatWarps) % slices_per_row == 0) --blocks;
+    }
     if (blocks > kMatMaxBlocks) blocks = kMatMaxBlocks;
     if (dtype == RLK_DTYPE_F32)
         k_mat_tile_partials<RLK_DTYPE_F32><<<static_cast<int>(blocks), kMatWarps * 32,
