@@ -58,9 +58,9 @@ constexpr int smem_bytes_of() {
 // stages as fit in a CTA's shared memory (227 KB) next to the barriers and,
 // for the backward, the G staging rows; at most kMaxStages.  A full 128-row
 // box gives the 4 stages above; the small boxes of decode batches (at most
-// 128 tokens, box rows roundup(T, 8)) give 5 up to 72 rows and 6 up to 40
-// (32 with the G staging): a deeper W stream where the MMAs are nearly
-// free.  Host and device compute it alike.
+// 128 tokens, box rows roundup(T, 8)) give 6 stages up to 40 rows and 5 up
+// to 104 (with the G staging: 16 and 72): a deeper W stream where the MMAs
+// are nearly free.  Host and device compute it alike.
 constexpr int kMaxStages = 6;
 constexpr int kSmemLimit = 232448;
 __host__ __device__ constexpr int ring_stages(int a_rows, bool grad) {
