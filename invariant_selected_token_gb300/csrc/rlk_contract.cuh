@@ -207,7 +207,13 @@ struct TreeX2 {
         float a, b, c, d;
         f2_unpack(e_lo, a, b);
         f2_unpack(e_hi, c, d);
-        x = f2_pack(__fadd_rn(a, b), __fadd_rn(c, d));  // X_j
+        push_node(j, f2_pack(__fadd_rn(a, b), __fadd_rn(c, d)));
+    }
+    // the level-1 node X_j = (s_j, s_j+32) itself, in order j = 0..31; with the
+    // exps formed on (column 2j, column 64+2j) and (2j+1, 64+2j+1) pairs, X_j
+    // is one packed add of the two
+    __device__ __forceinline__ void push_node(int j, uint64_t X) {
+        x = X;
         int level = 0;
 #pragma unroll
         for (; level < 5; ++level) {

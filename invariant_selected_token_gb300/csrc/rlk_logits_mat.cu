@@ -163,7 +163,10 @@ __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 b) {
 }
 
 // Second pass over a staged bf16 tile: the packed tree of the exps, reading
-// pairs j..j+3 and j+32..j+35 as they are needed.
+// pairs j..j+3 and j+32..j+35 as they are needed.  The exps run on (column
+// 2j, column 64+2j) and (2j+1, 64+2j+1) pairs, so the two level-1 sums s_j
+// and s_j+32 come out of one packed add (299.6 against 303.4 us with the
+// exps on (2j, 2j+1) pairs and two scalar adds).
 template <bool kUnderflow>
 __device__ __forceinline__ float bf16_tile_sum(const uint16_t* tile, uint64_t neg_m) {
     TreeX2 tree;
@@ -174,9 +177,13 @@ __device__ __forceinline__ float bf16_tile_sum(const uint16_t* tile, uint64_t ne
         const uint32_t L[4] = {lo.x, lo.y, lo.z, lo.w};
         const uint32_t H[4] = {hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            tree.push(j0 + i, contract_exp_x2<kUnderflow>(f2_add(widen_bf16x2(L[i]), neg_m)),
-                      contract_exp_x2<kUnderflow>(f2_add(widen_bf16x2(H[i]), neg_m)));
+        for (int i = 0; i < 4; ++i) {
+            const uint64_t even = f2_pack(__uint_as_float(L[i] << 16), __uint_as_float(H[i] << 16));
+            const uint64_t odd = f2_pack(__uint_as_float(L[i] & 0xFFFF0000u),
+                                         __uint_as_float(H[i] & 0xFFFF0000u));
+            tree.push_node(j0 + i, f2_add(contract_exp_x2<kUnderflow>(f2_add(even, neg_m)),
+                                          contract_exp_x2<kUnderflow>(f2_add(odd, neg_m))));
+        }
     }
     return tree.total();
 }
