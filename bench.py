@@ -46,13 +46,16 @@ def parse():
     p.add_argument("--workload", default="packed",
                    choices=["packed", "decode1", "decode8", "decode64", "decode128", "decode256",
                             "decode512",
-                            "logits_fp32", "logits_bf16", "log_softmax_fp32", "backward", "grpo",
+                            "logits_fp32", "logits_bf16", "log_softmax_fp32", "backward",
+                            "train_step", "grpo",
                             "rmsnorm", "rmsnorm16k", "sweep"],
                    help="packed: the T=4096 training batch (the headline); decodeN: N rows of it "
                         "as a rollout-side decode batch; logits_*: the same batch's logits "
                         "materialised in HBM, reduced by the materialised-logits path; "
                         "log_softmax_fp32: the full log_softmax [T, V] of those logits; "
-                        "backward: the deterministic backward of the packed batch; grpo: the "
+                        "backward: the deterministic backward of the packed batch; train_step: "
+                        "forward + backward of it, the forward saving its fp32 logits for the "
+                        "backward (the recomputing pair timed beside it); grpo: the "
                         "long-response GRPO batch (64 sequences, ~221 k rows in 8192-row calls); "
                         "rmsnorm: the strict RMSNorm (residual in and out) that produces the "
                         "packed batch's hidden states (L2 flushed between calls); rmsnorm16k: the "
@@ -814,6 +817,96 @@ def backward_arm(args, rank, world, dev, dist, W, pk, binding):
     return 0
 
 
+def train_step_arm(args, rank, world, dev, dist, W, pk, binding):
+    """One training step of the packed batch: forward (logprob, lse) and the backward of
+    sum_t g[t] logprob[t] (grad_hidden, grad_W).  Timed: the forward that saves its fp32
+    logits and the backward that forms G from them; beside it, in the same way, the
+    recomputing pair (plain forward, backward that runs the logits GEMM again).  Both give
+    the same bits; the line checks it."""
+    import torch
+    T = pk.hidden.shape[0]
+    g = torch.randn(T, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    ws_f = binding.new_workspace(T, V, N_SHARDS, dev)
+    ws_b = torch.empty(binding.backward_workspace_size(T, H, V), dtype=torch.uint8, device=dev)
+    logits = torch.empty((T, (V + 3) // 4 * 4), dtype=torch.float32, device=dev)
+    dh = torch.empty((T, H), dtype=torch.float32, device=dev)
+    dW = torch.empty((V, H), dtype=torch.float32, device=dev)
+    dh_r = torch.empty_like(dh)
+    dW_r = torch.empty_like(dW)
+    status = binding.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_saved():
+        _, lse, _ = binding.linear_logprob_save_logits(pk.hidden, W, pk.targets, None, N_SHARDS,
+                                                       logits=logits, workspace=ws_f,
+                                                       status=status, stream=stream)
+        binding.linear_logprob_backward_from_logits(logits, pk.hidden, W, pk.targets, g, lse,
+                                                    None, True, True, dh, dW, ws_b, status,
+                                                    stream)
+
+    def step_recompute():
+        _, lse = binding.linear_logprob(pk.hidden, W, pk.targets, None, N_SHARDS,
+                                        workspace=ws_f, status=status, stream=stream)
+        binding.linear_logprob_backward(pk.hidden, W, pk.targets, g, lse, None, True, True,
+                                        dh_r, dW_r, ws_b, status, stream)
+
+    K = max(1, args.steps // 4)
+    peaks = load_peaks()
+    out = {}
+    for name, step in (("recompute", step_recompute), ("saved", step_saved)):
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        binding.raise_on_device_status(status)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(dev.index or 0)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        s0.record(stream)
+        for _ in range(K):
+            step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        clk = clocks.stop(t0, time.time())
+        binding.raise_on_device_status(status)
+        out[name] = (max_over_ranks(s0.elapsed_time(s1), dist, dev), clk)
+    mismatch = int((dh.view(torch.int32) != dh_r.view(torch.int32)).sum().item() +
+                   (dW.view(torch.int32) != dW_r.view(torch.int32)).sum().item())
+    ms_total, clk = out["saved"]
+    ms = ms_total / K
+    flops = 3 * 2.0 * T * H * V  # forward, grad_hidden, grad_W
+    achieved = flops / (ms / 1000.0) / 1e12
+    if rank == 0:
+        line = {"metric": METRIC.replace("selected-logprob", "selected-logprob training step"),
+                "value": weak_scaling_value(world, T, K, ms_total), "unit": "tokens/s",
+                "n_gpus": world, "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": "training step of the packed batch (T=4096, H=4096, "
+                                       "V=151936): forward saving fp32 logits + backward from "
+                                       "them (grad_hidden, grad_W)", "T": T, "H": H, "V": V,
+                           "n_shards": N_SHARDS, "saved_logits_gb": round(logits.numel() * 4 / 1e9, 3),
+                           "recompute_ms_per_step": out["recompute"][0] / K,
+                           "recompute_clocks": out["recompute"][1],
+                           "grad_bits_vs_recompute": {"mismatch_count": mismatch}},
+                "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None,
+                             "kernel": "whole step (logits GEMM with the logits stored, G from "
+                                       "the logits, 2 GEMMs, split sum, tile tree)",
+                             "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)},
+                "cpu_baseline": None, "e2e": None, "gpu_launches": 6 * K, "clocks": clk,
+                "contract": binding.contract_id(), "build": binding.build_fingerprint()}
+        print(json.dumps(line))
+    if mismatch:
+        raise SystemExit("saved-logits backward differs from the recomputing one")
+    return 0
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -853,6 +946,8 @@ def main():
         return materialised_arm(args, rank, world, dev, dist, W, pk, binding, WL)
     if args.workload == "backward":
         return backward_arm(args, rank, world, dev, dist, W, pk, binding)
+    if args.workload == "train_step":
+        return train_step_arm(args, rank, world, dev, dist, W, pk, binding)
     if args.workload == "packed":
         hidden, targets = pk.hidden, pk.targets
         workload = WORKLOAD

@@ -305,6 +305,39 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
                                          int32_t* dev_status, rlk_stream_t stream);
 
 /*
+ * Training pair that trades memory for the backward's second logits GEMM:
+ * rlk_linear_logprob_save_logits is rlk_linear_logprob (same outputs, same
+ * bits) that also stores every row's fp32 logits (the exact accumulator
+ * values the epilogue reduces), and rlk_linear_logprob_backward_from_logits
+ * forms G from those stored logits instead of recomputing them, then runs
+ * the same two GEMMs: its grad_hidden and grad_W have the bits of
+ * rlk_linear_logprob_backward on the same batch.  Same backward definition
+ * as above (the blog's sections 3.3 and 4.2).
+ *
+ *   logits       device, float [T][ld_logits] row-major; written by the
+ *                forward (columns [0, V) of every row below T, active or
+ *                not), read by the backward; 16-byte aligned, ld_logits a
+ *                multiple of 4 and >= V (else RLK_ERR_ALIGNMENT /
+ *                RLK_ERR_INVALID_ARG); T * ld_logits * 4 bytes, owned by the
+ *                caller (2.49 GB at T = 4096, V = 151936)
+ * Forward: other arguments, outputs and errors as rlk_linear_logprob.
+ * Backward: other arguments, outputs and errors as rlk_linear_logprob_backward
+ * (hidden and W are still read: the GEMMs need them).
+ */
+rlk_status_t rlk_linear_logprob_save_logits(const void* hidden, const void* W,
+                                           const int32_t* targets, const uint8_t* active_mask,
+                                           int64_t T, int64_t H, int64_t V, int n_shards,
+                                           float* out_logprob, float* out_lse, float* logits,
+                                           int64_t ld_logits, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status,
+                                           rlk_stream_t stream);
+rlk_status_t rlk_linear_logprob_backward_from_logits(
+    const float* logits, int64_t ld_logits, const void* hidden, const void* W,
+    const int32_t* targets, const uint8_t* active_mask, const float* grad_logprob,
+    const float* lse, int64_t T, int64_t H, int64_t V, float* grad_hidden, float* grad_W,
+    void* workspace, size_t workspace_bytes, int32_t* dev_status, rlk_stream_t stream);
+
+/*
  * Strict RMSNorm producing the hidden states the head consumes (the
  * strict-path table's "RMSNorm" row: reduction domain, epsilon, residual
  * add, output boundary).  Per row:

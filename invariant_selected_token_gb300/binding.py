@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(HERE, "librlk.so")
 STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_INVALID_ARG", 2: "RLK_ERR_UNSUPPORTED",
                 3: "RLK_ERR_ALIGNMENT", 4: "RLK_ERR_WORKSPACE", 5: "RLK_ERR_CUDA",
                 6: "RLK_ERR_TARGET_RANGE", 7: "RLK_ERR_TIMEOUT"}
+RLK_ERR_INVALID_ARG = 1
+RLK_ERR_ALIGNMENT = 3
 RLK_ERR_TARGET_RANGE = 6
 RLK_ERR_TIMEOUT = 7
 VOCAB_TILE = 128
@@ -30,7 +32,8 @@ EXPORTED = ["rlk_contract_id", "rlk_build_fingerprint", "rlk_status_string", "rl
             "rlk_lse_merge", "rlk_tile_partials", "rlk_tile_merge", "rlk_debug_logits",
             "rlk_linear_logprob_static_ws", "rlk_logits_logprob", "rlk_log_softmax",
             "rlk_backward_workspace_size", "rlk_linear_logprob_backward", "rlk_rmsnorm",
-            "rlk_debug_primitive_hash"]
+            "rlk_debug_primitive_hash", "rlk_linear_logprob_save_logits",
+            "rlk_linear_logprob_backward_from_logits"]
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 
@@ -81,6 +84,12 @@ def lib() -> ctypes.CDLL:
         L.rlk_linear_logprob_backward.restype = i32
         L.rlk_linear_logprob_backward.argtypes = [P, P, P, P, P, P, i64, i64, i64, P, P, P, sz, P,
                                                   P]
+        L.rlk_linear_logprob_save_logits.restype = i32
+        L.rlk_linear_logprob_save_logits.argtypes = [P, P, P, P, i64, i64, i64, i32, P, P, P, i64,
+                                                     P, sz, P, P]
+        L.rlk_linear_logprob_backward_from_logits.restype = i32
+        L.rlk_linear_logprob_backward_from_logits.argtypes = [P, i64, P, P, P, P, P, P, i64, i64,
+                                                              i64, P, P, P, sz, P, P]
         L.rlk_rmsnorm.restype = i32
         L.rlk_rmsnorm.argtypes = [P, P, P, ctypes.c_float, i64, i64, P, P, P]
         L.rlk_log_softmax.restype = i32
@@ -373,6 +382,74 @@ def linear_logprob_backward(hidden, W, targets, grad_logprob, lse, active=None,
             _ptr(grad_hidden if want_hidden else None), _ptr(grad_W if want_W else None),
             _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
             "rlk_linear_logprob_backward")
+    return (grad_hidden if want_hidden else None), (grad_W if want_W else None)
+
+
+def linear_logprob_save_logits(hidden, W, targets, active=None, n_shards: int = 1, logits=None,
+                               workspace=None, status=None, stream=None):
+    """(logprob [T], lse [T], logits fp32 [T, ld]): rlk_linear_logprob's outputs and bits,
+    plus every row's fp32 logits for rlk_linear_logprob_backward_from_logits.  `logits`, if
+    given, is a float32 [T, ld] tensor with ld >= V a multiple of 4 (its first V columns are
+    written)."""
+    dev = hidden.device
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W, torch.bfloat16, "W", dev, ndim=2)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    if active is not None:
+        _require(active, torch.uint8, "active", dev, ndim=1)
+    T, H = hidden.shape
+    V = W.shape[0]
+    if W.shape[1] != H or targets.shape[0] != T or (active is not None and active.shape[0] != T):
+        raise ValueError("shape mismatch")
+    if logits is None:
+        logits = torch.empty((T, (V + 3) // 4 * 4), dtype=torch.float32, device=dev)
+    _require(logits, torch.float32, "logits", dev, ndim=2)
+    if logits.stride(1) != 1 or logits.shape[0] != T:
+        raise ValueError("logits must be [T, ld] with unit column stride")
+    out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, V, n_shards, dev)
+    with _on(dev):
+        _check(lib().rlk_linear_logprob_save_logits(
+            _ptr(hidden), _ptr(W), _ptr(targets), _ptr(active), T, H, V, n_shards,
+            _ptr(out_logprob), _ptr(out_lse), _ptr(logits), logits.stride(0), _ptr(workspace),
+            workspace.numel(), _ptr(status), _stream(dev, stream)),
+            "rlk_linear_logprob_save_logits")
+    return out_logprob, out_lse, logits
+
+
+def linear_logprob_backward_from_logits(logits, hidden, W, targets, grad_logprob, lse,
+                                        active=None, want_hidden: bool = True,
+                                        want_W: bool = True, grad_hidden=None, grad_W=None,
+                                        workspace=None, status=None, stream=None):
+    """linear_logprob_backward with G formed from the saved fp32 logits [T, ld] of
+    linear_logprob_save_logits (same bits)."""
+    dev = hidden.device
+    _require(logits, torch.float32, "logits", dev, ndim=2)
+    _require(hidden, torch.bfloat16, "hidden", ndim=2)
+    _require(W, torch.bfloat16, "W", dev, ndim=2)
+    _require(targets, torch.int32, "targets", dev, ndim=1)
+    _require(grad_logprob, torch.float32, "grad_logprob", dev, ndim=1)
+    _require(lse, torch.float32, "lse", dev, ndim=1)
+    T, H = hidden.shape
+    V = W.shape[0]
+    if logits.stride(1) != 1 or logits.shape[0] != T:
+        raise ValueError("logits must be [T, ld] with unit column stride")
+    if want_hidden and grad_hidden is None:
+        grad_hidden = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if want_W and grad_W is None:
+        grad_W = torch.empty((V, H), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(256, backward_workspace_size(T, H, V)), dtype=torch.uint8,
+                                device=dev)
+    with _on(dev):
+        _check(lib().rlk_linear_logprob_backward_from_logits(
+            _ptr(logits), logits.stride(0), _ptr(hidden), _ptr(W), _ptr(targets), _ptr(active),
+            _ptr(grad_logprob), _ptr(lse), T, H, V,
+            _ptr(grad_hidden if want_hidden else None), _ptr(grad_W if want_W else None),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev, stream)),
+            "rlk_linear_logprob_backward_from_logits")
     return (grad_hidden if want_hidden else None), (grad_W if want_W else None)
 
 

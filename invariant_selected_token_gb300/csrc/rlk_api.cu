@@ -165,10 +165,13 @@ int test_drop_stage_code() {
 }
 bool test_drop_stage() { return test_drop_stage_code() == 1; }
 
+// logits_out (with its row stride ld_logits): the saving forward, which
+// also stores every row's fp32 logits; dbg: the debug dump (logits only).
 rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t* targets,
                                const uint8_t* active, int64_t T, int64_t H, int64_t V_local,
                                int64_t v_offset, float2* partials, float* tgt, float* dbg,
-                               int32_t* status, cudaStream_t stream, const DeviceState* dev) {
+                               int32_t* status, cudaStream_t stream, const DeviceState* dev,
+                               float* logits_out = nullptr, int64_t ld_logits = 0) {
     CUtensorMap map_h, map_w;
     // one token tile: load only the rows that exist (rounded up to a whole
     // 8-row swizzle atom); the MMA's other accumulator rows are discarded
@@ -196,9 +199,12 @@ rlk_status_t run_tile_partials(const void* hidden, const void* W, const int32_t*
     a.G = nullptr;
     a.ldG = 0;
     a.V_total = V_local;
-    return rlk::launch_tile_partials(map_h, map_w, a,
-                                     dbg != nullptr ? rlk::kEpiDebugLogits : rlk::kEpiPartials,
-                                     dev->sm_count, stream) == cudaSuccess
+    a.logits_out = logits_out;
+    a.ld_logits = ld_logits;
+    const int epi = dbg != nullptr ? rlk::kEpiDebugLogits
+                    : logits_out != nullptr ? rlk::kEpiSave
+                                            : rlk::kEpiPartials;
+    return rlk::launch_tile_partials(map_h, map_w, a, epi, dev->sm_count, stream) == cudaSuccess
                ? RLK_OK
                : RLK_ERR_CUDA;
 }
@@ -305,6 +311,93 @@ rlk_status_t mat_checks(const void* logits, int dtype, int64_t ld, int64_t T, in
     return RLK_OK;
 }
 
+// Argument checks shared by the two backward calls (T == 0 passes).
+rlk_status_t backward_checks(const void* hidden, const void* W, const int32_t* targets,
+                             const float* grad_logprob, const float* lse, int64_t T, int64_t H,
+                             int64_t V, const float* grad_hidden, const float* grad_W,
+                             const void* workspace, size_t workspace_bytes) {
+    rlk_status_t s = common_checks(hidden, W, targets, T, H);
+    if (s != RLK_OK) return s;
+    if (V < 1) return RLK_ERR_INVALID_ARG;
+    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
+    if (T == 0) return RLK_OK;
+    if (!grad_logprob || !lse || !workspace || (!grad_hidden && !grad_W))
+        return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(grad_logprob, 4) || !aligned(lse, 4) ||
+        !aligned(grad_hidden, 4) || !aligned(grad_W, 4))
+        return RLK_ERR_ALIGNMENT;
+    if (workspace_bytes < backward_layout_of(T, H, V).total) return RLK_ERR_WORKSPACE;
+    return RLK_OK;
+}
+
+// Steps 2 and 3 of both backward calls: the two GEMMs from G.
+rlk_status_t backward_gemms(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
+                            uint16_t* G, int64_t ldG, uint8_t* parts, float* grad_hidden,
+                            float* grad_W, int32_t* dev_status, cudaStream_t st,
+                            const DeviceState* dev) {
+    rlk_status_t s = RLK_OK;
+    // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum.
+    //    Feature tiles fastest, in bands of 8: the ~152 CTAs running together cover about
+    //    19 token tiles x 8 feature tiles of one K range, sharing each G slice (19 k
+    //    columns) and each W slice through L2.  Against all 16 feature tiles per band
+    //    (9.5 token tiles at a time), each wave re-reads less of the range's W slice, which
+    //    is larger than L2: at T = 4096, 5.76 GB of DRAM reads instead of 6.60 GB.
+    if (grad_hidden) {
+        CUtensorMap map_g, map_wmn;
+        if ((s = encode_bf16_k_map(&map_g, G, V, T, ldG, kTileM)) != RLK_OK) return s;
+        if ((s = encode_bf16_mn_map(&map_wmn, W, H, V, H)) != RLK_OK) return s;
+        const int kb = int((V + rlk::kBlockK - 1) / rlk::kBlockK);
+        const int splits = kb < kGradHiddenSplits ? kb : kGradHiddenSplits;
+        rlk::GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.out = reinterpret_cast<float*>(parts);
+        g.ld_out = H;
+        g.split_stride = T * H;
+        g.M = int(T);
+        g.N = int(H);
+        g.k_blocks = kb;
+        g.kb_per_split = (kb + splits - 1) / splits;
+        g.splits = (kb + g.kb_per_split - 1) / g.kb_per_split;
+        g.vec_store = true;
+        g.n_fastest = true;
+        g.n_band = 8;
+        g.test_drop_stage = test_drop_stage_code() == 2 ? 1 : 0;
+        g.status = dev_status;
+        if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+        if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
+                                   dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+    }
+
+    // 3. grad_W = G^T h: K = T ascending, one range
+    if (grad_W) {
+        CUtensorMap map_gt, map_hmn;
+        if ((s = encode_bf16_mn_map(&map_gt, G, V, T, ldG)) != RLK_OK) return s;
+        if ((s = encode_bf16_mn_map(&map_hmn, hidden, H, T, H)) != RLK_OK) return s;
+        rlk::GemmArgs g;
+        std::memset(&g, 0, sizeof(g));
+        g.out = grad_W;
+        g.ld_out = H;
+        g.split_stride = 0;
+        g.M = int(V);
+        g.N = int(H);
+        g.k_blocks = int((T + rlk::kBlockK - 1) / rlk::kBlockK);
+        g.kb_per_split = g.k_blocks;
+        g.splits = 1;
+        g.vec_store = aligned(grad_W, 16);
+        // bands of hidden-feature tiles whose hidden columns take ~32 MB of L2
+        const int64_t band_bytes = int64_t(32) << 20;
+        const int64_t per_tile = T * 256 * 2;  // one 256-feature tile of the T hidden rows
+        g.n_band = int(band_bytes / per_tile > 1 ? band_bytes / per_tile : 1);
+        g.n_fastest = true;
+        g.status = dev_status;
+        if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)
+            return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -403,6 +496,36 @@ rlk_status_t rlk_linear_logprob(const void* hidden, const void* W, const int32_t
     if (s != RLK_OK) return s;
     return rlk_tile_merge(targets, active_mask, T, V, n_shards, out_logprob, out_lse, workspace,
                           workspace_bytes, dev_status, stream);
+}
+
+rlk_status_t rlk_linear_logprob_save_logits(const void* hidden, const void* W,
+                                           const int32_t* targets, const uint8_t* active_mask,
+                                           int64_t T, int64_t H, int64_t V, int n_shards,
+                                           float* out_logprob, float* out_lse, float* logits,
+                                           int64_t ld_logits, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status,
+                                           rlk_stream_t stream) {
+    rlk_status_t s = common_checks(hidden, W, targets, T, H);
+    if (s != RLK_OK) return s;
+    if ((s = shard_check(V, n_shards)) != RLK_OK) return s;
+    if (T == 0) return RLK_OK;
+    if (!out_logprob || !out_lse || !logits || !workspace || ld_logits < V)
+        return RLK_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256) || !aligned(logits, 16) || ld_logits % 4 != 0)
+        return RLK_ERR_ALIGNMENT;
+    const Layout l = layout_of(T, V, n_shards);
+    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    s = run_tile_partials(hidden, W, targets, active_mask, T, H, V, 0,
+                          reinterpret_cast<float2*>(ws + l.partials),
+                          reinterpret_cast<float*>(ws + l.tgt), nullptr, dev_status, st, dev,
+                          logits, ld_logits);
+    if (s != RLK_OK) return s;
+    return run_tile_tree(targets, active_mask, T, V, n_shards, out_logprob, out_lse, ws, l,
+                         dev_status, st, dev);
 }
 
 rlk_status_t rlk_linear_logprob_shard(const void* hidden, const void* W_shard,
@@ -567,22 +690,14 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
                                          int64_t H, int64_t V, float* grad_hidden, float* grad_W,
                                          void* workspace, size_t workspace_bytes,
                                          int32_t* dev_status, rlk_stream_t stream) {
-    rlk_status_t s = common_checks(hidden, W, targets, T, H);
-    if (s != RLK_OK) return s;
-    if (V < 1) return RLK_ERR_INVALID_ARG;
-    if (V > RLK_MAX_VOCAB) return RLK_ERR_UNSUPPORTED;
-    if (T == 0) return RLK_OK;
-    if (!grad_logprob || !lse || !workspace || (!grad_hidden && !grad_W))
-        return RLK_ERR_INVALID_ARG;
-    if (!aligned(workspace, 256) || !aligned(grad_logprob, 4) || !aligned(lse, 4) ||
-        !aligned(grad_hidden, 4) || !aligned(grad_W, 4))
-        return RLK_ERR_ALIGNMENT;
-    const BackwardLayout l = backward_layout_of(T, H, V);
-    if (workspace_bytes < l.total) return RLK_ERR_WORKSPACE;
+    rlk_status_t s = backward_checks(hidden, W, targets, grad_logprob, lse, T, H, V, grad_hidden,
+                                     grad_W, workspace, workspace_bytes);
+    if (s != RLK_OK || T == 0) return s;
     DeviceState* dev = nullptr;
     if ((s = device_check(&dev)) != RLK_OK) return s;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const BackwardLayout l = backward_layout_of(T, H, V);
     uint16_t* G = reinterpret_cast<uint16_t*>(ws + l.G);
     const int64_t ldG = grad_ld(V);
 
@@ -610,67 +725,34 @@ rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,
     if (rlk::launch_tile_partials(map_h, map_w, a, rlk::kEpiGrad, dev->sm_count, st) !=
         cudaSuccess)
         return RLK_ERR_CUDA;
+    return backward_gemms(hidden, W, T, H, V, G, ldG, ws + l.parts, grad_hidden, grad_W,
+                          dev_status, st, dev);
+}
 
-    // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum.
-    //    Feature tiles fastest, in bands of 8: the ~152 CTAs running together cover about
-    //    19 token tiles x 8 feature tiles of one K range, sharing each G slice (19 k
-    //    columns) and each W slice through L2.  Against all 16 feature tiles per band
-    //    (9.5 token tiles at a time), each wave re-reads less of the range's W slice, which
-    //    is larger than L2: at T = 4096, 5.76 GB of DRAM reads instead of 6.60 GB.
-    if (grad_hidden) {
-        CUtensorMap map_g, map_wmn;
-        if ((s = encode_bf16_k_map(&map_g, G, V, T, ldG, kTileM)) != RLK_OK) return s;
-        if ((s = encode_bf16_mn_map(&map_wmn, W, H, V, H)) != RLK_OK) return s;
-        const int kb = int((V + rlk::kBlockK - 1) / rlk::kBlockK);
-        const int splits = kb < kGradHiddenSplits ? kb : kGradHiddenSplits;
-        rlk::GemmArgs g;
-        std::memset(&g, 0, sizeof(g));
-        g.out = reinterpret_cast<float*>(ws + l.parts);
-        g.ld_out = H;
-        g.split_stride = T * H;
-        g.M = int(T);
-        g.N = int(H);
-        g.k_blocks = kb;
-        g.kb_per_split = (kb + splits - 1) / splits;
-        g.splits = (kb + g.kb_per_split - 1) / g.kb_per_split;
-        g.vec_store = true;
-        g.n_fastest = true;
-        g.n_band = 8;
-        g.test_drop_stage = test_drop_stage_code() == 2 ? 1 : 0;
-        g.status = dev_status;
-        if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
-            return RLK_ERR_CUDA;
-        if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
-                                   dev->sm_count, st) != cudaSuccess)
-            return RLK_ERR_CUDA;
-    }
-
-    // 3. grad_W = G^T h: K = T ascending, one range
-    if (grad_W) {
-        CUtensorMap map_gt, map_hmn;
-        if ((s = encode_bf16_mn_map(&map_gt, G, V, T, ldG)) != RLK_OK) return s;
-        if ((s = encode_bf16_mn_map(&map_hmn, hidden, H, T, H)) != RLK_OK) return s;
-        rlk::GemmArgs g;
-        std::memset(&g, 0, sizeof(g));
-        g.out = grad_W;
-        g.ld_out = H;
-        g.split_stride = 0;
-        g.M = int(V);
-        g.N = int(H);
-        g.k_blocks = int((T + rlk::kBlockK - 1) / rlk::kBlockK);
-        g.kb_per_split = g.k_blocks;
-        g.splits = 1;
-        g.vec_store = aligned(grad_W, 16);
-        // bands of hidden-feature tiles whose hidden columns take ~32 MB of L2
-        const int64_t band_bytes = int64_t(32) << 20;
-        const int64_t per_tile = T * 256 * 2;  // one 256-feature tile of the T hidden rows
-        g.n_band = int(band_bytes / per_tile > 1 ? band_bytes / per_tile : 1);
-        g.n_fastest = true;
-        g.status = dev_status;
-        if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)
-            return RLK_ERR_CUDA;
-    }
-    return RLK_OK;
+rlk_status_t rlk_linear_logprob_backward_from_logits(
+    const float* logits, int64_t ld_logits, const void* hidden, const void* W,
+    const int32_t* targets, const uint8_t* active_mask, const float* grad_logprob,
+    const float* lse, int64_t T, int64_t H, int64_t V, float* grad_hidden, float* grad_W,
+    void* workspace, size_t workspace_bytes, int32_t* dev_status, rlk_stream_t stream) {
+    rlk_status_t s = backward_checks(hidden, W, targets, grad_logprob, lse, T, H, V, grad_hidden,
+                                     grad_W, workspace, workspace_bytes);
+    if (s != RLK_OK || T == 0) return s;
+    if (!logits || ld_logits < V) return RLK_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || ld_logits % 4 != 0) return RLK_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    if ((s = device_check(&dev)) != RLK_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const BackwardLayout l = backward_layout_of(T, H, V);
+    uint16_t* G = reinterpret_cast<uint16_t*>(ws + l.G);
+    const int64_t ldG = grad_ld(V);
+    // 1. G = g (onehot - softmax) in bf16 from the saved logits (the forward's lse)
+    if (rlk::launch_grad_from_logits(logits, ld_logits, targets, active_mask, grad_logprob, lse,
+                                     int(T), int(V), G, ldG, dev_status, dev->sm_count,
+                                     st) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return backward_gemms(hidden, W, T, H, V, G, ldG, ws + l.parts, grad_hidden, grad_W,
+                          dev_status, st, dev);
 }
 
 rlk_status_t rlk_rmsnorm(const void* x, const void* residual, const void* gamma, float eps,

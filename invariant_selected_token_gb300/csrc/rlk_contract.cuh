@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <math_constants.h>
 
 namespace rlk {
@@ -145,6 +146,25 @@ __device__ __forceinline__ uint64_t contract_exp_x2(uint64_t x) {
     f2_unpack(f2_mul(p, scale), yl, yh);
     f2_unpack(x, xl, xh);
     return f2_pack(xl < -86.0f ? 0.0f : yl, xh < -86.0f ? 0.0f : yh);
+}
+
+// Two columns of the logit gradient G = bf16_RN(RN(g * d)), d = RN(1 - p) at
+// the target and -p elsewhere, p = contract_exp(RN(l - lse)), from the fp32
+// logits (l0, l1) as one packed pair; neg_lse = (-lse, -lse), g2 = (g, g).
+// Returns the two bf16 values, the first in the low half.  Rows that take no
+// part pass valid = false and get zeros.
+__device__ __forceinline__ uint32_t contract_grad_x2(uint64_t l01, uint64_t neg_lse, uint64_t g2,
+                                                     bool tgt0, bool tgt1, bool valid) {
+    float p0, p1;
+    f2_unpack(contract_exp_x2(f2_add(l01, neg_lse)), p0, p1);
+    const float d0 = tgt0 ? __fsub_rn(1.0f, p0) : -p0;
+    const float d1 = tgt1 ? __fsub_rn(1.0f, p1) : -p1;
+    float g0, g1;
+    f2_unpack(f2_mul(g2, f2_pack(d0, d1)), g0, g1);
+    if (!valid) g0 = g1 = 0.0f;
+    const __nv_bfloat162 b = __floats2bfloat162_rn(g0, g1);  // round each to nearest
+    return static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
 }
 
 // rsqrt(a) for positive normal a: Lomont's seed for the bit-level inverse

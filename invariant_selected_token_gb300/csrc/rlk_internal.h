@@ -37,9 +37,13 @@ struct TilePartialsArgs {
     uint16_t* G;              // bf16 [T][ldG] logit gradient
     int64_t ldG;
     int64_t V_total;          // for the target-range check
+    // saving forward only: the fp32 logits [T][ld_logits] (16-byte aligned, ld % 4 == 0)
+    float* logits_out;
+    int64_t ld_logits;
 };
 
-enum TileEpilogue { kEpiPartials = 0, kEpiDebugLogits = 1, kEpiGrad = 2 };
+// kEpiSave: kEpiPartials plus every row's fp32 logits stored for the backward
+enum TileEpilogue { kEpiPartials = 0, kEpiDebugLogits = 1, kEpiGrad = 2, kEpiSave = 3 };
 
 // hidden map: bf16 [T][H], box 64 x a_box_rows; weight map: bf16 [V_local][H], box 64 x 256.
 cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
@@ -82,6 +86,12 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
 // Sets the kernels' shared-memory limits and reports the CTAs per SM of
 // k_mat_tile_partials for fp32 [0] and bf16 [1] logits.
 cudaError_t prepare_mat_kernels(int* ctas_per_sm);
+// G[t][v] (bf16, row stride ldG) from fp32 logits [T][ld] (16-byte aligned, ld % 4 == 0):
+// the backward epilogue's arithmetic on the saved logits instead of recomputed ones
+cudaError_t launch_grad_from_logits(const float* logits, int64_t ld, const int32_t* targets,
+                                    const uint8_t* active, const float* grad, const float* lse,
+                                    int T, int V, uint16_t* G, int64_t ldG, int32_t* status,
+                                    int num_sms, cudaStream_t stream);
 // out[t][v] = RN(l[t][v] - lse[t])
 cudaError_t launch_log_softmax_out(const void* logits, int dtype, int64_t ld, const float* lse,
                                    const uint8_t* active, int T, int V, float* out, int num_sms,

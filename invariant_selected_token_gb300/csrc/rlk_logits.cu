@@ -49,9 +49,14 @@ constexpr int kSmemBytes = kStages * (kStageBytesA + kStageBytesB) + 1024 /*alig
 // access phase touches fall in distinct bank quads.
 constexpr int kGradPitch = 72;
 constexpr uint32_t kGradStageBytes = 4 * 32 * kGradPitch * 2;  // 18 KB
+// The saving forward turns 32 rows x 32 columns of fp32 logits around the
+// same way (pitch 36 floats, again 144 bytes) in the same 18 KB.
+constexpr int kSavePitch = 36;
+static_assert(4 * 32 * kSavePitch * 4 == kGradStageBytes, "one staging region for both");
+__host__ __device__ constexpr bool staged_epi(int epi) { return epi == kEpiGrad || epi == kEpiSave; }
 template <int kEpi>
 constexpr int smem_bytes_of() {
-    return kSmemBytes + (kEpi == kEpiGrad ? static_cast<int>(kGradStageBytes) : 0);
+    return kSmemBytes + (staged_epi(kEpi) ? static_cast<int>(kGradStageBytes) : 0);
 }
 
 // Ring depth for a hidden box of `a_rows` rows: as many (hidden box, W box)
@@ -70,8 +75,8 @@ __host__ __device__ constexpr int ring_stages(int a_rows, bool grad) {
 }
 template <int kEpi>
 constexpr int ring_smem_bytes(int a_rows) {
-    return ring_stages(a_rows, kEpi == kEpiGrad) * (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB)) +
-           1024 + 256 + (kEpi == kEpiGrad ? static_cast<int>(kGradStageBytes) : 0);
+    return ring_stages(a_rows, staged_epi(kEpi)) * (a_rows * kBlockK * 2 + static_cast<int>(kStageBytesB)) +
+           1024 + 256 + (staged_epi(kEpi) ? static_cast<int>(kGradStageBytes) : 0);
 }
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
@@ -124,16 +129,8 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
         for (int i = 0; i < 4; ++i) {
             // columns c, c + 1, two per instruction with the scalar bits
             const int c = q * 8 + 2 * i;
-            float p0, p1;
-            f2_unpack(contract_exp_x2(f2_add(f2_pack(v[c], v[c + 1]), neg_lse)), p0, p1);
-            const float d0 = (c == tl) ? __fsub_rn(1.0f, p0) : -p0;
-            const float d1 = (c + 1 == tl) ? __fsub_rn(1.0f, p1) : -p1;
-            float g0, g1;
-            f2_unpack(f2_mul(g2, f2_pack(d0, d1)), g0, g1);
-            if (!valid) g0 = g1 = 0.0f;
-            const __nv_bfloat162 b = __floats2bfloat162_rn(g0, g1);  // round each to nearest
-            w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(b.x)) |
-                   (static_cast<uint32_t>(__bfloat16_as_ushort(b.y)) << 16);
+            w[i] = contract_grad_x2(f2_pack(v[c], v[c + 1]), neg_lse, g2, c == tl, c + 1 == tl,
+                                    valid);
         }
         if (staged) {
             *reinterpret_cast<uint4*>(stage + lane * kGradPitch + (q % 8) * 8) =
@@ -161,6 +158,43 @@ __device__ __forceinline__ void grad_tile(const float (&v)[kVocabTile], const Ti
                                               half * 64 + ch * 8) = x;
             }
             __syncwarp();  // the staging rows are free for the next half
+        }
+    }
+}
+
+// Saving forward: the tile's fp32 logits (its ncols real columns) into
+// logits_out row t.  Called by the whole warp (lane = row0 + lane's row):
+// each full 32-column quarter goes through the warp's staging rows and out
+// in 128-byte row segments; a ragged last quarter is stored element by
+// element.  Rows at or beyond T store nothing.
+__device__ __forceinline__ void save_tile(const float (&v)[kVocabTile], const TilePartialsArgs& a,
+                                          int t, int c0, int ncols, float* stage, int lane,
+                                          int row0) {
+#pragma unroll
+    for (int q = 0; q < kVocabTile / 32; ++q) {
+        if (q * 32 + 32 <= ncols) {  // the same for the whole warp
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<float4*>(stage + lane * kSavePitch + 4 * k) =
+                    make_float4(v[q * 32 + 4 * k], v[q * 32 + 4 * k + 1], v[q * 32 + 4 * k + 2],
+                                v[q * 32 + 4 * k + 3]);
+            __syncwarp();
+            // lanes 8j..8j+7 store row 4i + j, 16 bytes each
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const int ch = lane & 7;
+                const float4 x = *reinterpret_cast<const float4*>(stage + r * kSavePitch + ch * 4);
+                if (row0 + r < a.T)
+                    *reinterpret_cast<float4*>(a.logits_out + static_cast<int64_t>(row0 + r) * a.ld_logits +
+                                               c0 + q * 32 + ch * 4) = x;
+            }
+            __syncwarp();  // the staging rows are free for the next quarter
+        } else if (t < a.T) {
+            float* dst = a.logits_out + static_cast<int64_t>(t) * a.ld_logits + c0;
+#pragma unroll
+            for (int c = q * 32; c < q * 32 + 32; ++c)
+                if (c < ncols) dst[c] = v[c];
         }
     }
 }
@@ -204,7 +238,7 @@ __device__ __forceinline__ UnitCoords unit_coords(int unit, int num_n, int num_m
 //               shared by two CTAs and streamed from HBM while their MMAs run at
 //               the same pace, and the extra W stage of lookahead pays
 //               (232 -> 224 us at T = 256); at the tensor-bound sizes it cost
-//               8 %, so no other size uses it.  Not with the backward's G
+//               8 %, so no other size uses it.  Not with the G or logits
 //               staging rows, which leave no room for the fifth W stage.
 enum RingKind { kRingFull = 0, kRingSmall = 1, kRingSplit = 2 };
 constexpr int kSplitStagesB = kStages + 1;
@@ -223,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // hidden slots are a_box_rows rows each; the MMA still reads 128 rows from a
     // slot, and the rows past the box (the next slots' or the W boxes' bytes,
     // inside this allocation) only feed accumulator rows that are never read
-    const int S = kRing == kRingSmall ? ring_stages(a.a_box_rows, kEpi == kEpiGrad) : kStages;
+    const int S = kRing == kRingSmall ? ring_stages(a.a_box_rows, staged_epi(kEpi)) : kStages;
     const int SB = kSplit ? kSplitStagesB : S;  // W slots
     const uint32_t a_stage = kRing == kRingSmall
                                  ? static_cast<uint32_t>(a.a_box_rows) * kBlockK * 2
@@ -240,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    // backward only: per-epilogue-warp staging rows for the G stores
+    // backward and saving forward only: per-epilogue-warp staging rows for
+    // the G or logits stores
     uint16_t* grad_stage = reinterpret_cast<uint16_t*>(sB + SB * kStageBytesB + 256);
 
     const int warp = threadIdx.x >> 5;
@@ -455,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kEpi == kEpiGrad && valid && n_blk == 0 && (tg_local < 0 || tg_local >= a.V_total))
                 report(a.status, RLK_ERR_TARGET_RANGE);
             if (__any_sync(0xffffffffu, kEpi == kEpiPartials ? valid : (t < a.T))) {
+                // kEpiSave: every row below T stores its logits, active or not
 #pragma unroll 1
                 for (int sub = 0; sub < kTileN / kVocabTile; ++sub) {
                     const int j = n_blk * (kTileN / kVocabTile) + sub;
@@ -485,6 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   m_blk * kTileM + quad * 32);
                         continue;
                     }
+                    if (kEpi == kEpiSave)
+                        save_tile(v, a, t, c0, ncols,
+                                  reinterpret_cast<float*>(grad_stage) + quad * (32 * kSavePitch),
+                                  lane, m_blk * kTileM + quad * 32);
                     const int64_t tl = tg_local - c0;
                     const bool own = valid && tl >= 0 && tl < ncols;
                     if (__any_sync(0xffffffffu, own)) {
@@ -533,7 +573,7 @@ cudaError_t set_smem_attr() {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_tile_partials<kEpi, kRingSmall>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    if constexpr (kEpi != kEpiGrad) {
+    if constexpr (!staged_epi(kEpi)) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_tile_partials<kEpi, kRingSplit>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmemBytes);
@@ -552,7 +592,7 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     const int ring = a.a_box_rows < kTileM ? kRingSmall
-                     : (num_m == 2 && kEpi != kEpiGrad) ? kRingSplit
+                     : (num_m == 2 && !staged_epi(kEpi)) ? kRingSplit
                                                          : kRingFull;
     cfg.dynamicSmemBytes = ring == kRingSmall ? ring_smem_bytes<kEpi>(a.a_box_rows)
                            : ring == kRingSplit ? kSplitSmemBytes
@@ -565,7 +605,7 @@ cudaError_t launch_epi(const CUtensorMap& map_hidden, const CUtensorMap& map_w,
     cfg.numAttrs = 1;
     if (ring == kRingSmall)
         return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, kRingSmall>, map_hidden, map_w, a);
-    if constexpr (kEpi != kEpiGrad) {
+    if constexpr (!staged_epi(kEpi)) {
         if (ring == kRingSplit)
             return cudaLaunchKernelEx(&cfg, k_tile_partials<kEpi, kRingSplit>, map_hidden, map_w, a);
     }
@@ -578,6 +618,7 @@ cudaError_t prepare_tile_partials_kernels() {
     cudaError_t e;
     if ((e = set_smem_attr<kEpiPartials>()) != cudaSuccess) return e;
     if ((e = set_smem_attr<kEpiDebugLogits>()) != cudaSuccess) return e;
+    if ((e = set_smem_attr<kEpiSave>()) != cudaSuccess) return e;
     return set_smem_attr<kEpiGrad>();
 }
 
@@ -587,6 +628,7 @@ cudaError_t launch_tile_partials(const CUtensorMap& map_hidden, const CUtensorMa
     if (epilogue == kEpiDebugLogits)
         return launch_epi<kEpiDebugLogits>(map_hidden, map_w, a, num_sms, stream);
     if (epilogue == kEpiGrad) return launch_epi<kEpiGrad>(map_hidden, map_w, a, num_sms, stream);
+    if (epilogue == kEpiSave) return launch_epi<kEpiSave>(map_hidden, map_w, a, num_sms, stream);
     return launch_epi<kEpiPartials>(map_hidden, map_w, a, num_sms, stream);
 }
 

@@ -363,6 +363,55 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// The backward's G from saved fp32 logits: one thread per 8 columns of a row
+// (two 16-byte loads, one 16-byte store), the arithmetic of the fused
+// gradient epilogue (contract_grad_x2) on the same fp32 logits, so G has the
+// same bits.  Inactive rows get zeros; an active row whose target is out of
+// range sets RLK_ERR_TARGET_RANGE (its G has no target column).
+__global__ void __launch_bounds__(256)
+    k_grad_from_logits(const float* logits, int64_t ld, const int32_t* targets,
+                       const uint8_t* active, const float* grad, const float* lse, int T, int V,
+                       uint16_t* G, int64_t ldG, int32_t* status) {
+    const int64_t groups_per_row = (V + 7) / 8;
+    const int64_t n = static_cast<int64_t>(T) * groups_per_row;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(i / groups_per_row);
+        const int c = static_cast<int>(i - static_cast<int64_t>(t) * groups_per_row) * 8;
+        const bool valid = active ? active[t] != 0 : true;
+        const int64_t tg = targets[t];
+        if (valid && c == 0 && (tg < 0 || tg >= V) && status)
+            atomicOr(status, 1 << RLK_ERR_TARGET_RANGE);
+        const int64_t tl = tg - c;
+        const uint64_t neg_lse = f2_splat(valid ? -lse[t] : 0.0f);
+        const uint64_t g2 = f2_splat(valid ? grad[t] : 0.0f);
+        const float* src = logits + static_cast<int64_t>(t) * ld + c;
+        float x[8];
+        if (c + 8 <= V) {
+            const float4 a = *reinterpret_cast<const float4*>(src);
+            const float4 b = *reinterpret_cast<const float4*>(src + 4);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = c + k < V ? src[k] : 0.0f;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = contract_grad_x2(f2_pack(x[2 * k], x[2 * k + 1]), neg_lse, g2, 2 * k == tl,
+                                    2 * k + 1 == tl, valid);
+        uint16_t* dst = G + static_cast<int64_t>(t) * ldG + c;
+        if (c + 8 <= V) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (c + k < V) dst[k] = static_cast<uint16_t>(w[k / 2] >> (16 * (k & 1)));
+        }
+    }
+}
+
 // one slice per warp: fp32 4 warps x 32 tiles x 132 x 4 B = 66 KB (3 CTAs per
 // SM), bf16 4 x 32 x 136 x 2 B = 34 KB (6 CTAs per SM)
 template <int kDtype>
@@ -431,6 +480,20 @@ cudaError_t launch_mat_tile_partials(const void* logits, int dtype, int64_t ld,
         k_mat_tile_partials<RLK_DTYPE_BF16><<<static_cast<int>(blocks), kMatWarps * 32,
                                               mat_smem_bytes<RLK_DTYPE_BF16>(), stream>>>(logits, ld, vec, targets, active, T, V,
                                                         n_tiles, partials, tgt_logit);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_from_logits(const float* logits, int64_t ld, const int32_t* targets,
+                                    const uint8_t* active, const float* grad, const float* lse,
+                                    int T, int V, uint16_t* G, int64_t ldG, int32_t* status,
+                                    int num_sms, cudaStream_t stream) {
+    const int64_t n = static_cast<int64_t>(T) * ((V + 7) / 8);
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    k_grad_from_logits<<<static_cast<int>(blocks), 256, 0, stream>>>(logits, ld, targets, active,
+                                                                     grad, lse, T, V, G, ldG,
+                                                                     status);
     return cudaGetLastError();
 }
 
