@@ -147,6 +147,40 @@ def test_materialised_logits_validation(L):
     assert g(0x10001, 0, 1001, None, 4, 1000, 0x40000, 0x50000, 0x60000, 1 << 20, None, None) == 3
 
 
+def test_training_pair_validation(L):
+    # the saving forward and the backward from saved logits: host checks only
+    f = L.rlk_linear_logprob_save_logits
+    ok = dict(h=0x10000, W=0x20000, tg=0x30000, T=4, H=64, V=1000, n=1, lp=0x40000, lse=0x50000,
+              lg=0x70000, ld=1000, ws=0x60000, wsb=1 << 20)
+
+    def fwd(**kw):
+        a = dict(ok, **kw)
+        return f(a["h"], a["W"], a["tg"], None, a["T"], a["H"], a["V"], a["n"], a["lp"], a["lse"],
+                 a["lg"], a["ld"], a["ws"], a["wsb"], None, None)
+    assert fwd(lg=None) == 1
+    assert fwd(ld=996) == 1           # ld < V
+    assert fwd(ld=1002) == 3          # rows must start on 16-byte boundaries
+    assert fwd(lg=0x70008) == 3
+    assert fwd(n=3) == 2
+    assert fwd(wsb=10) == 4
+    assert fwd(T=0) == 0
+    b = L.rlk_linear_logprob_backward_from_logits
+    okb = dict(lg=0x70000, ld=1000, h=0x10000, W=0x20000, tg=0x30000, g=0x40000, lse=0x50000, T=4,
+               H=64, V=1000, dh=0x80000, dW=0x90000, ws=0x60000, wsb=1 << 30)
+
+    def bwd(**kw):
+        a = dict(okb, **kw)
+        return b(a["lg"], a["ld"], a["h"], a["W"], a["tg"], None, a["g"], a["lse"], a["T"], a["H"],
+                 a["V"], a["dh"], a["dW"], a["ws"], a["wsb"], None, None)
+    assert bwd(lg=None) == 1
+    assert bwd(ld=999) == 1
+    assert bwd(ld=1001) == 3
+    assert bwd(lg=0x70004) == 3
+    assert bwd(dh=None, dW=None) == 1
+    assert bwd(wsb=10) == 4
+    assert bwd(T=0) == 0
+
+
 def test_rmsnorm_validation(L):
     f = L.rlk_rmsnorm
     import ctypes as C
