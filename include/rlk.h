@@ -295,6 +295,12 @@ rlk_status_t rlk_log_softmax(const void* logits, int logits_dtype, int64_t ld,
  * Inactive rows contribute nothing (their G row is zero).  An active row
  * whose target lies outside [0, V) sets RLK_ERR_TARGET_RANGE and gets no
  * one-hot term.  Other arguments as rlk_linear_logprob.
+ * When both gradients are asked for, grad_hidden's fixed-order split sum
+ * runs beside the grad_W GEMM on a library stream, forked from `stream`
+ * after grad_hidden's GEMM and joined back before the call's work on
+ * `stream` ends (events; capturable in a CUDA graph).  The first such call
+ * on a device creates that stream and its two events; they live for the
+ * process.
  */
 size_t rlk_backward_workspace_size(int64_t T, int64_t H, int64_t V);
 rlk_status_t rlk_linear_logprob_backward(const void* hidden, const void* W,

@@ -35,6 +35,12 @@ struct DeviceState {
     int sm_count = 0;
     int cc = 0;             // 10 * major + minor
     int mat_ctas_per_sm[2] = {0, 0};  // materialised-logits kernel, fp32 / bf16
+    // backward: grad_hidden's split sum runs on this stream beside the grad_W
+    // GEMM (created at the first backward that computes both); `side_mutex`
+    // keeps one call's record / wait sequence on the two events whole
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_split = nullptr, ev_sum = nullptr;
+    std::mutex side_mutex;
 };
 
 std::mutex g_mutex;
@@ -330,11 +336,41 @@ rlk_status_t backward_checks(const void* hidden, const void* W, const int32_t* t
     return RLK_OK;
 }
 
+// Step 3 of both backward calls: grad_W = G^T h (K = T ascending, one range).
+rlk_status_t grad_w_gemm(const void* hidden, int64_t T, int64_t H, int64_t V, uint16_t* G,
+                         int64_t ldG, float* grad_W, int32_t* dev_status, cudaStream_t st,
+                         const DeviceState* dev) {
+    rlk_status_t s = RLK_OK;
+    CUtensorMap map_gt, map_hmn;
+    if ((s = encode_bf16_mn_map(&map_gt, G, V, T, ldG)) != RLK_OK) return s;
+    if ((s = encode_bf16_mn_map(&map_hmn, hidden, H, T, H)) != RLK_OK) return s;
+    rlk::GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.out = grad_W;
+    g.ld_out = H;
+    g.split_stride = 0;
+    g.M = int(V);
+    g.N = int(H);
+    g.k_blocks = int((T + rlk::kBlockK - 1) / rlk::kBlockK);
+    g.kb_per_split = g.k_blocks;
+    g.splits = 1;
+    g.vec_store = aligned(grad_W, 16);
+    // bands of hidden-feature tiles whose hidden columns take ~32 MB of L2
+    const int64_t band_bytes = int64_t(32) << 20;
+    const int64_t per_tile = T * 256 * 2;  // one 256-feature tile of the T hidden rows
+    g.n_band = int(band_bytes / per_tile > 1 ? band_bytes / per_tile : 1);
+    g.n_fastest = true;
+    g.status = dev_status;
+    if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    return RLK_OK;
+}
+
 // Steps 2 and 3 of both backward calls: the two GEMMs from G.
 rlk_status_t backward_gemms(const void* hidden, const void* W, int64_t T, int64_t H, int64_t V,
                             uint16_t* G, int64_t ldG, uint8_t* parts, float* grad_hidden,
                             float* grad_W, int32_t* dev_status, cudaStream_t st,
-                            const DeviceState* dev) {
+                            DeviceState* dev) {
     rlk_status_t s = RLK_OK;
     // 2. grad_hidden = G W: K = V in kGradHiddenSplits fixed ranges, then a fixed-order sum.
     //    Feature tiles fastest, in bands of 8: the ~152 CTAs running together cover about
@@ -365,36 +401,35 @@ rlk_status_t backward_gemms(const void* hidden, const void* W, int64_t T, int64_
         g.status = dev_status;
         if (rlk::launch_gemm_f32(map_g, map_wmn, false, true, g, dev->sm_count, st) != cudaSuccess)
             return RLK_ERR_CUDA;
-        if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
-                                   dev->sm_count, st) != cudaSuccess)
-            return RLK_ERR_CUDA;
+        if (!grad_W) {
+            if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
+                                       dev->sm_count, st) != cudaSuccess)
+                return RLK_ERR_CUDA;
+        } else {
+            // the memory-bound split sum beside the tensor-bound grad_W GEMM, on the
+            // side stream: forked after grad_hidden's GEMM, joined after grad_W's
+            std::lock_guard<std::mutex> lock(dev->side_mutex);
+            if (!dev->side) {
+                if (cudaStreamCreateWithFlags(&dev->side, cudaStreamNonBlocking) != cudaSuccess ||
+                    cudaEventCreateWithFlags(&dev->ev_split, cudaEventDisableTiming) != cudaSuccess ||
+                    cudaEventCreateWithFlags(&dev->ev_sum, cudaEventDisableTiming) != cudaSuccess)
+                    return RLK_ERR_CUDA;
+            }
+            if (cudaEventRecord(dev->ev_split, st) != cudaSuccess ||
+                cudaStreamWaitEvent(dev->side, dev->ev_split, 0) != cudaSuccess)
+                return RLK_ERR_CUDA;
+            if (rlk::launch_sum_splits(g.out, g.split_stride, g.splits, T * H, grad_hidden,
+                                       dev->sm_count, dev->side) != cudaSuccess ||
+                cudaEventRecord(dev->ev_sum, dev->side) != cudaSuccess)
+                return RLK_ERR_CUDA;
+            s = grad_w_gemm(hidden, T, H, V, G, ldG, grad_W, dev_status, st, dev);
+            if (cudaStreamWaitEvent(st, dev->ev_sum, 0) != cudaSuccess) return RLK_ERR_CUDA;
+            return s;
+        }
     }
 
     // 3. grad_W = G^T h: K = T ascending, one range
-    if (grad_W) {
-        CUtensorMap map_gt, map_hmn;
-        if ((s = encode_bf16_mn_map(&map_gt, G, V, T, ldG)) != RLK_OK) return s;
-        if ((s = encode_bf16_mn_map(&map_hmn, hidden, H, T, H)) != RLK_OK) return s;
-        rlk::GemmArgs g;
-        std::memset(&g, 0, sizeof(g));
-        g.out = grad_W;
-        g.ld_out = H;
-        g.split_stride = 0;
-        g.M = int(V);
-        g.N = int(H);
-        g.k_blocks = int((T + rlk::kBlockK - 1) / rlk::kBlockK);
-        g.kb_per_split = g.k_blocks;
-        g.splits = 1;
-        g.vec_store = aligned(grad_W, 16);
-        // bands of hidden-feature tiles whose hidden columns take ~32 MB of L2
-        const int64_t band_bytes = int64_t(32) << 20;
-        const int64_t per_tile = T * 256 * 2;  // one 256-feature tile of the T hidden rows
-        g.n_band = int(band_bytes / per_tile > 1 ? band_bytes / per_tile : 1);
-        g.n_fastest = true;
-        g.status = dev_status;
-        if (rlk::launch_gemm_f32(map_gt, map_hmn, true, true, g, dev->sm_count, st) != cudaSuccess)
-            return RLK_ERR_CUDA;
-    }
+    if (grad_W) return grad_w_gemm(hidden, T, H, V, G, ldG, grad_W, dev_status, st, dev);
     return RLK_OK;
 }
 
